@@ -54,12 +54,14 @@ def residual_row(p_row_logits, q_row_logits):
     return r
 
 
-def spec_sample(p_logits, q_logits, draft_tokens, seed, offset=0):
+def spec_sample(p_logits, q_logits, draft_tokens, seed, offset=0, seq_ids=None):
     """Exact speculative sampling of N independent drafted blocks.
 
     p_logits     [N or 1][k+1][V] target logits for positions 1..k+1
     q_logits     [N or 1][k][V]   draft logits for positions 1..k
     draft_tokens [N][k]           drafted tokens x_1..x_k
+    seq_ids      [N] sequence indices used as the Philox counter's first word
+                 (default 0..N-1; a subset of a larger batch keeps its ids)
     returns out_tokens [N][k+1] int64 (accepted drafts, then the correcting or
             bonus token, then -1 padding), n_accepted [N] int64, and a dict of
             the intermediate quantities (ratios, uniforms, residual totals)
@@ -72,15 +74,19 @@ def spec_sample(p_logits, q_logits, draft_tokens, seed, offset=0):
     pn = np.arange(N) if p.shape[0] == N else np.zeros(N, dtype=np.int64)
     qn = np.arange(N) if q.shape[0] == N else np.zeros(N, dtype=np.int64)
     n = np.arange(N)
+    cn = n if seq_ids is None else np.asarray(seq_ids, dtype=np.int64)
     pos = np.arange(k)
 
     px = p[pn[:, None], pos[None, :], x]
     qx = q[qn[:, None], pos[None, :], x]
     with np.errstate(divide="ignore"):
         ratio = px / qx
-    u_acc = philox_uniform(seed, offset, n[:, None], pos[None, :], STREAM_ACCEPT)
+    u_acc = philox_uniform(seed, offset, cn[:, None], pos[None, :], STREAM_ACCEPT)
     accepted = u_acc < ratio
-    n_acc = np.where(accepted.all(axis=1), k, np.argmin(accepted, axis=1))
+    if k == 0:
+        n_acc = np.zeros(N, dtype=np.int64)
+    else:
+        n_acc = np.where(accepted.all(axis=1), k, np.argmin(accepted, axis=1))
 
     # Row to sample from: residual at the first rejection, else p_{k+1}.
     rej = n_acc < k
@@ -94,7 +100,7 @@ def spec_sample(p_logits, q_logits, draft_tokens, seed, offset=0):
         row[rej] = r
     cdf = np.cumsum(row, axis=1)
     total = cdf[:, -1]
-    u_res = philox_uniform(seed, offset, n, n_acc, STREAM_RESAMPLE)
+    u_res = philox_uniform(seed, offset, cn, n_acc, STREAM_RESAMPLE)
     target = u_res * total
     y = np.argmax(cdf > target[:, None], axis=1)
 

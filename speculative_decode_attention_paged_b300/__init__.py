@@ -1,0 +1,292 @@
+"""Python binding of the S³R paged decode-attention library (libs3r.so).
+
+Argument marshalling only: every function here takes torch tensors, checks
+that they are contiguous CUDA tensors of the right dtype, and passes their
+device pointers and sizes to the C entry point of the same name declared in
+include/s3r.h.  All computation happens in the CUDA kernels of libs3r.so;
+there is no CPU fallback.  If the library has not been built the first call
+raises (build it with ``python -m speculative_decode_attention_paged_b300.build``).
+"""
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "S3RError",
+    "S3RDeviceError",
+    "PagedKVDesc",
+    "Workspace",
+    "lib_path",
+    "load_library",
+    "s3r_version",
+    "s3r_attn_workspace_size",
+    "s3r_spec_sample_workspace_size",
+    "s3r_select_workspace_size",
+    "s3r_dense_decode_attn",
+    "s3r_sparse_draft_attn",
+    "s3r_verify_attn",
+    "s3r_select_draft_pages",
+    "s3r_spec_sample",
+    "DEVERR_BAD_PAGE",
+    "DEVERR_BAD_LENGTH",
+    "DEVERR_BAD_TOKEN",
+    "DEVERR_TIMEOUT",
+    "DEVERR_BAD_COUNT",
+]
+
+PAGE_SIZE = 16
+HEAD_DIM = 128
+MAX_ROWS_PER_KV_HEAD = 32
+
+DEVERR_BAD_PAGE = 0x1
+DEVERR_BAD_LENGTH = 0x2
+DEVERR_BAD_TOKEN = 0x4
+DEVERR_TIMEOUT = 0x8
+DEVERR_BAD_COUNT = 0x10
+
+_STATUS = {0: "S3R_OK", 1: "S3R_ERR_INVALID_ARG", 2: "S3R_ERR_UNSUPPORTED", 3: "S3R_ERR_CUDA",
+           4: "S3R_ERR_WORKSPACE"}
+
+
+class S3RError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} returned {_STATUS.get(status, status)}")
+
+
+class S3RDeviceError(RuntimeError):
+    def __init__(self, code):
+        self.code = code
+        super().__init__(f"device error word 0x{code:x}")
+
+
+class _PagedKV(ctypes.Structure):
+    _fields_ = [
+        ("k_pool", ctypes.c_void_p),
+        ("v_pool", ctypes.c_void_p),
+        ("num_phys_pages", ctypes.c_int64),
+        ("block_table", ctypes.c_void_p),
+        ("max_pages_per_seq", ctypes.c_int32),
+        ("num_seqs", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+    ]
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SIG = {
+    "s3r_version": (ctypes.c_char_p, []),
+    "s3r_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "s3r_attn_workspace_size": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _I32, ctypes.POINTER(ctypes.c_size_t)]),
+    "s3r_spec_sample_workspace_size": (ctypes.c_int, [_I32, _I32, ctypes.POINTER(ctypes.c_size_t)]),
+    "s3r_select_workspace_size": (ctypes.c_int, [ctypes.POINTER(ctypes.c_size_t)]),
+    "s3r_workspace_init": (ctypes.c_int, [_P, ctypes.c_size_t, _P]),
+    "s3r_read_device_error": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32), _I32]),
+    "s3r_dense_decode_attn": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _P, _P, ctypes.c_float, _P,
+                                             ctypes.c_size_t, _P]),
+    "s3r_sparse_draft_attn": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _I32, _P, _P, _I32, _P, _P,
+                                             ctypes.c_float, _P, ctypes.c_size_t, _P]),
+    "s3r_verify_attn": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _I32, _P, _P, _P, _I32, ctypes.c_float,
+                                       _P, ctypes.c_size_t, _P]),
+    "s3r_select_draft_pages": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, ctypes.c_double, _I32, _I32, _P, _P,
+                                              _I32, _P, ctypes.c_size_t, _P]),
+    "s3r_spec_sample": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64, _P, _P,
+                                       _P, ctypes.c_size_t, _P]),
+}
+
+_lib = None
+
+
+def lib_path():
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libs3r.so")
+
+
+def load_library():
+    """Load libs3r.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m speculative_decode_attention_paged_b300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIG.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _call(name, *args):
+    status = getattr(load_library(), name)(*args)
+    if status != 0:
+        raise S3RError(name, status)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class PagedKVDesc:
+    """Descriptor of one layer's paged KV cache (device tensors stay owned by
+    the caller and must outlive the descriptor's use)."""
+
+    def __init__(self, k_pool, v_pool, block_table, num_q_heads):
+        _need(k_pool, torch.bfloat16, "k_pool")
+        _need(v_pool, torch.bfloat16, "v_pool")
+        _need(block_table, torch.int32, "block_table")
+        if k_pool.shape != v_pool.shape or k_pool.dim() != 4:
+            raise ValueError("k_pool and v_pool must both be [pages][kv_heads][16][head_dim]")
+        self.k_pool, self.v_pool, self.block_table = k_pool, v_pool, block_table
+        self.num_q_heads = int(num_q_heads)
+        self.c = _PagedKV(
+            k_pool=k_pool.data_ptr(), v_pool=v_pool.data_ptr(), num_phys_pages=k_pool.shape[0],
+            block_table=block_table.data_ptr(), max_pages_per_seq=block_table.shape[1],
+            num_seqs=block_table.shape[0], num_q_heads=self.num_q_heads, num_kv_heads=k_pool.shape[1],
+            head_dim=k_pool.shape[3], page_size=k_pool.shape[2])
+
+    @property
+    def num_seqs(self):
+        return self.c.num_seqs
+
+    @property
+    def num_kv_heads(self):
+        return self.c.num_kv_heads
+
+    @property
+    def max_pages(self):
+        return self.c.max_pages_per_seq
+
+
+class Workspace:
+    """Caller-owned device scratch buffer for the library (error word first)."""
+
+    def __init__(self, nbytes, device=None, stream=None):
+        nbytes = max(int(nbytes), 256)
+        self.buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.buf.data_ptr()) % 256
+        self.view = self.buf[off: off + nbytes]
+        self.nbytes = nbytes
+        _call("s3r_workspace_init", _ptr(self.view), ctypes.c_size_t(nbytes), _stream(stream))
+
+    def ptr(self):
+        return _ptr(self.view)
+
+    def read_error(self, clear=True, stream=None):
+        code = _I32(0)
+        _call("s3r_read_device_error", self.ptr(), _stream(stream), ctypes.byref(code), _I32(1 if clear else 0))
+        return code.value
+
+    def check(self, stream=None):
+        code = self.read_error(clear=True, stream=stream)
+        if code:
+            raise S3RDeviceError(code)
+
+
+def s3r_version():
+    return load_library().s3r_version().decode()
+
+
+def s3r_attn_workspace_size(kv: PagedKVDesc, max_block_rows=1):
+    n = ctypes.c_size_t(0)
+    _call("s3r_attn_workspace_size", ctypes.byref(kv.c), _I32(max_block_rows), ctypes.byref(n))
+    return n.value
+
+
+def s3r_spec_sample_workspace_size(n, k):
+    out = ctypes.c_size_t(0)
+    _call("s3r_spec_sample_workspace_size", _I32(n), _I32(k), ctypes.byref(out))
+    return out.value
+
+
+def s3r_select_workspace_size():
+    out = ctypes.c_size_t(0)
+    _call("s3r_select_workspace_size", ctypes.byref(out))
+    return out.value
+
+
+def s3r_dense_decode_attn(kv: PagedKVDesc, ctx_lens, q, out, sm_scale, ws: Workspace, stream=None):
+    _need(ctx_lens, torch.int32, "ctx_lens")
+    _need(q, torch.bfloat16, "q")
+    _need(out, torch.float32, "out")
+    _call("s3r_dense_decode_attn", ctypes.byref(kv.c), _ptr(ctx_lens), _ptr(q), _ptr(out),
+          ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return out
+
+
+def s3r_sparse_draft_attn(kv: PagedKVDesc, hist_lens, draft_pos, sel_pages, sel_count, q, out, sm_scale,
+                          ws: Workspace, stream=None):
+    _need(hist_lens, torch.int32, "hist_lens")
+    _need(sel_pages, torch.int32, "sel_pages")
+    _need(sel_count, torch.int32, "sel_count")
+    _need(q, torch.bfloat16, "q")
+    _need(out, torch.float32, "out")
+    _call("s3r_sparse_draft_attn", ctypes.byref(kv.c), _ptr(hist_lens), _I32(draft_pos), _ptr(sel_pages),
+          _ptr(sel_count), _I32(sel_pages.shape[-1]), _ptr(q), _ptr(out), ctypes.c_float(sm_scale),
+          ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return out
+
+
+def s3r_verify_attn(kv: PagedKVDesc, hist_lens, q, out, sm_scale, ws: Workspace, page_mass=None, stream=None):
+    _need(hist_lens, torch.int32, "hist_lens")
+    _need(q, torch.bfloat16, "q")
+    _need(out, torch.float32, "out")
+    stride = 0
+    if page_mass is not None:
+        _need(page_mass, torch.float32, "page_mass")
+        stride = page_mass.shape[-1]
+    _call("s3r_verify_attn", ctypes.byref(kv.c), _ptr(hist_lens), _I32(q.shape[1]), _ptr(q), _ptr(out),
+          _ptr(page_mass), _I32(stride), ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes),
+          _stream(stream))
+    return out
+
+
+def s3r_select_draft_pages(page_mass, sel_lens, budget, sel_pages, sel_count, ws: Workspace, n_sink=1,
+                           n_recent=4, stream=None):
+    _need(page_mass, torch.float32, "page_mass")
+    _need(sel_lens, torch.int32, "sel_lens")
+    _need(sel_pages, torch.int32, "sel_pages")
+    _need(sel_count, torch.int32, "sel_count")
+    S, Hkv, stride = page_mass.shape
+    _call("s3r_select_draft_pages", _ptr(page_mass), _ptr(sel_lens), _I32(S), _I32(Hkv), _I32(stride),
+          ctypes.c_double(budget), _I32(n_sink), _I32(n_recent), _ptr(sel_pages), _ptr(sel_count),
+          _I32(sel_pages.shape[-1]), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return sel_pages, sel_count
+
+
+def s3r_spec_sample(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, n_accepted, ws: Workspace,
+                    stream=None):
+    _need(p_logits, torch.float32, "p_logits")
+    _need(q_logits, torch.float32, "q_logits")
+    _need(draft_tokens, torch.int32, "draft_tokens")
+    _need(out_tokens, torch.int32, "out_tokens")
+    _need(n_accepted, torch.int32, "n_accepted")
+    n, k1, V = p_logits.shape
+    _call("s3r_spec_sample", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1), _I32(V),
+          ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), ws.ptr(),
+          ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return out_tokens, n_accepted

@@ -1,0 +1,306 @@
+// C ABI of the S³R hot path: host-side validation, workspace layout, TMA
+// descriptors and kernel launches.  Declarations and contracts: include/s3r.h.
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "attn_paged.cuh"
+#include "s3r_device.cuh"
+
+namespace s3r {
+cudaError_t launch_select_pages(const float* mass, const int32_t* sel_lens, int S, int Hkv,
+                                int stride, double budget, int n_sink, int n_recent,
+                                int32_t* sel_pages, int32_t* sel_count, int b_max, int* err,
+                                cudaStream_t stream);
+cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
+                               int V, uint64_t seed, uint32_t offset, float2* stats,
+                               int32_t* out_tokens, int32_t* n_accepted, int* err,
+                               cudaStream_t stream);
+}  // namespace s3r
+
+namespace {
+
+using namespace s3r;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSpecK = 64;
+
+int g_sm_count[kMaxDevices];
+std::once_flag g_encode_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+// SM count of the current device (cached), or 0 on failure.
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  });
+  return g_encode;
+}
+
+// 3-D view of a KV pool: (d: 128, row: kv_heads*16, page: num_phys_pages);
+// box (64, 16, 1) = one 64-column half of a (page, KV head) tile, 128B swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int kv_heads, int64_t num_pages) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kv_heads) * kPage,
+                        static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                           static_cast<cuuint64_t>(kv_heads) * kPage * kHeadDim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kPage), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+s3r_status validate_kv(const s3r_paged_kv* kv) {
+  if (kv == nullptr) return S3R_ERR_INVALID_ARG;
+  if (kv->head_dim != kHeadDim || kv->page_size != kPage) return S3R_ERR_UNSUPPORTED;
+  if (kv->num_seqs < 0 || kv->num_kv_heads <= 0 || kv->num_q_heads <= 0 ||
+      kv->max_pages_per_seq <= 0 || kv->num_phys_pages <= 0)
+    return S3R_ERR_INVALID_ARG;
+  if (kv->num_q_heads % kv->num_kv_heads != 0) return S3R_ERR_INVALID_ARG;
+  if (kv->num_phys_pages > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(kv->max_pages_per_seq) * kPage > 0x3fffffff) return S3R_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(kv->num_seqs) * kv->num_kv_heads > kMaxPairs) return S3R_ERR_UNSUPPORTED;
+  if (kv->num_seqs > 0) {
+    if (kv->k_pool == nullptr || kv->v_pool == nullptr || kv->block_table == nullptr)
+      return S3R_ERR_INVALID_ARG;
+    if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return S3R_ERR_INVALID_ARG;
+  }
+  return S3R_OK;
+}
+
+s3r_status to_status(cudaError_t e) { return e == cudaSuccess ? S3R_OK : S3R_ERR_CUDA; }
+
+// Shared body of the three attention calls.
+s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, int T,
+                         int draft_pos, const int32_t* sel_pages, const int32_t* sel_count,
+                         int b_max, const void* q, void* out, float* page_mass, int mass_stride,
+                         float sm_scale, void* ws, size_t ws_bytes, void* stream) {
+  s3r_status st = validate_kv(kv);
+  if (st != S3R_OK) return st;
+  if (!std::isfinite(sm_scale)) return S3R_ERR_INVALID_ARG;
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  const int R = T * G;
+  if (T <= 0) return S3R_ERR_INVALID_ARG;
+  if (R > S3R_MAX_ROWS_PER_KV_HEAD) return S3R_ERR_UNSUPPORTED;
+  if (ws == nullptr || !aligned256(ws)) return S3R_ERR_WORKSPACE;
+  if (kv->num_seqs == 0) return S3R_OK;
+  if (lens == nullptr || q == nullptr || out == nullptr) return S3R_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return S3R_ERR_INVALID_ARG;
+  if (mode == kModeSparse) {
+    if (draft_pos < 0 || b_max < 0 || (b_max > 0 && sel_pages == nullptr) || sel_count == nullptr)
+      return S3R_ERR_INVALID_ARG;
+  }
+  const bool mass = page_mass != nullptr;
+  if (mass && mass_stride < kv->max_pages_per_seq) return S3R_ERR_INVALID_ARG;
+
+  const int sms = current_sm_count();
+  if (sms <= 0) return S3R_ERR_CUDA;
+  const int total_warps = sms * kAttnWarps;
+  const int n_pairs = kv->num_seqs * kv->num_kv_heads;
+  const AttnWorkspaceLayout lay =
+      attn_workspace_layout(n_pairs, R, kv->max_pages_per_seq, total_warps, mass);
+  if (ws_bytes < lay.total) return S3R_ERR_WORKSPACE;
+
+  CUtensorMap kmap, vmap;
+  if (!encode_pool_map(&kmap, kv->k_pool, kv->num_kv_heads, kv->num_phys_pages) ||
+      !encode_pool_map(&vmap, kv->v_pool, kv->num_kv_heads, kv->num_phys_pages))
+    return S3R_ERR_CUDA;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  AttnArgs a{};
+  a.mode = mode;
+  a.S = kv->num_seqs;
+  a.Hq = kv->num_q_heads;
+  a.Hkv = kv->num_kv_heads;
+  a.G = G;
+  a.T = T;
+  a.R = R;
+  a.max_pages = kv->max_pages_per_seq;
+  a.num_phys_pages = kv->num_phys_pages;
+  a.block_table = kv->block_table;
+  a.lens = lens;
+  a.draft_pos = draft_pos;
+  a.sel_pages = sel_pages;
+  a.sel_count = sel_count;
+  a.b_max = b_max;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.out = static_cast<float*>(out);
+  a.scale_log2 = sm_scale * kLog2e;
+  a.page_mass = page_mass;
+  a.mass_stride = mass_stride;
+  a.err = reinterpret_cast<int*>(w + lay.err_off);
+  a.chunk_prefix = reinterpret_cast<int*>(w + lay.prefix_off);
+  a.part_o = reinterpret_cast<float*>(w + lay.part_o_off);
+  a.part_ml = reinterpret_cast<float*>(w + lay.part_ml_off);
+  a.row_lse = mass ? reinterpret_cast<float*>(w + lay.row_lse_off) : nullptr;
+  a.page_lse = mass ? reinterpret_cast<float*>(w + lay.page_lse_off) : nullptr;
+  a.total_warps = total_warps;
+  a.n_pairs = n_pairs;
+  a.n_chunks = (n_pairs + kPairChunk - 1) / kPairChunk;
+  return to_status(launch_attention(kmap, vmap, a, sms, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* s3r_version(void) { return "s3r-b300 0.1.0 (sm_103a)"; }
+
+const char* s3r_status_string(s3r_status status) {
+  switch (status) {
+    case S3R_OK: return "S3R_OK";
+    case S3R_ERR_INVALID_ARG: return "S3R_ERR_INVALID_ARG";
+    case S3R_ERR_UNSUPPORTED: return "S3R_ERR_UNSUPPORTED";
+    case S3R_ERR_CUDA: return "S3R_ERR_CUDA";
+    case S3R_ERR_WORKSPACE: return "S3R_ERR_WORKSPACE";
+  }
+  return "S3R_UNKNOWN_STATUS";
+}
+
+s3r_status s3r_attn_workspace_size(const s3r_paged_kv* kv, int32_t max_block_rows, size_t* bytes) {
+  if (bytes == nullptr) return S3R_ERR_INVALID_ARG;
+  s3r_status st = validate_kv(kv);
+  if (st != S3R_OK) return st;
+  if (max_block_rows <= 0) return S3R_ERR_INVALID_ARG;
+  const int G = kv->num_q_heads / kv->num_kv_heads;
+  const int64_t R = static_cast<int64_t>(max_block_rows) * G;
+  if (R > S3R_MAX_ROWS_PER_KV_HEAD) return S3R_ERR_UNSUPPORTED;
+  const int sms = current_sm_count();
+  if (sms <= 0) return S3R_ERR_CUDA;
+  *bytes = attn_workspace_layout(kv->num_seqs * kv->num_kv_heads, static_cast<int>(R),
+                                 kv->max_pages_per_seq, sms * kAttnWarps, true)
+               .total;
+  return S3R_OK;
+}
+
+s3r_status s3r_spec_sample_workspace_size(int32_t n, int32_t k, size_t* bytes) {
+  if (bytes == nullptr || n < 0 || k < 0) return S3R_ERR_INVALID_ARG;
+  if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
+  *bytes = 256 + ((static_cast<size_t>(n) * (2 * k + 1) * sizeof(float2) + 255) & ~size_t(255));
+  return S3R_OK;
+}
+
+s3r_status s3r_select_workspace_size(size_t* bytes) {
+  if (bytes == nullptr) return S3R_ERR_INVALID_ARG;
+  *bytes = 256;
+  return S3R_OK;
+}
+
+s3r_status s3r_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return S3R_ERR_WORKSPACE;
+  return to_status(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));
+}
+
+s3r_status s3r_read_device_error(const void* ws, void* stream, int32_t* code, int32_t clear) {
+  if (ws == nullptr || code == nullptr) return S3R_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return S3R_ERR_CUDA;
+  *code = v;
+  if (clear) {
+    e = cudaMemsetAsync(const_cast<void*>(ws), 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return S3R_ERR_CUDA;
+  }
+  return S3R_OK;
+}
+
+s3r_status s3r_dense_decode_attn(const s3r_paged_kv* kv, const int32_t* ctx_lens, const void* q,
+                                 void* out, float sm_scale, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return run_attention(kv, kModeDense, ctx_lens, 1, 0, nullptr, nullptr, 0, q, out, nullptr, 0,
+                       sm_scale, ws, ws_bytes, stream);
+}
+
+s3r_status s3r_sparse_draft_attn(const s3r_paged_kv* kv, const int32_t* hist_lens,
+                                 int32_t draft_pos, const int32_t* sel_pages,
+                                 const int32_t* sel_count, int32_t b_max, const void* q, void* out,
+                                 float sm_scale, void* ws, size_t ws_bytes, void* stream) {
+  return run_attention(kv, kModeSparse, hist_lens, 1, draft_pos, sel_pages, sel_count, b_max, q,
+                       out, nullptr, 0, sm_scale, ws, ws_bytes, stream);
+}
+
+s3r_status s3r_verify_attn(const s3r_paged_kv* kv, const int32_t* hist_lens, int32_t n_rows,
+                           const void* q, void* out, float* page_mass, int32_t mass_stride,
+                           float sm_scale, void* ws, size_t ws_bytes, void* stream) {
+  return run_attention(kv, kModeVerify, hist_lens, n_rows, 0, nullptr, nullptr, 0, q, out,
+                       page_mass, mass_stride, sm_scale, ws, ws_bytes, stream);
+}
+
+s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t* sel_lens, int32_t num_seqs,
+                                  int32_t num_kv_heads, int32_t mass_stride, double budget,
+                                  int32_t n_sink, int32_t n_recent, int32_t* sel_pages,
+                                  int32_t* sel_count, int32_t b_max, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (num_seqs < 0 || num_kv_heads <= 0 || mass_stride <= 0 || n_sink < 0 || n_recent < 0 ||
+      b_max < 0)
+    return S3R_ERR_INVALID_ARG;
+  if (!(budget >= 0.0 && budget <= 1.0)) return S3R_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return S3R_ERR_WORKSPACE;
+  if (static_cast<int64_t>(num_seqs) * num_kv_heads > 0x7fffffff) return S3R_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return S3R_OK;
+  if (page_mass == nullptr || sel_lens == nullptr || sel_pages == nullptr || sel_count == nullptr)
+    return S3R_ERR_INVALID_ARG;
+  // The page budget grows with the history; the longest history the mass
+  // rows can describe is mass_stride pages.
+  const int P = mass_stride;
+  const int n_mand = std::min(n_sink, P) + (P - std::max(std::max(P - n_recent, 0), std::min(n_sink, P)));
+  const double want = std::ceil(budget * static_cast<double>(P) - 1e-9);
+  const int B = static_cast<int>(std::min(static_cast<double>(P), std::max(want, static_cast<double>(n_mand))));
+  if (b_max < B) return S3R_ERR_INVALID_ARG;
+  return to_status(launch_select_pages(page_mass, sel_lens, num_seqs, num_kv_heads, mass_stride,
+                                       budget, n_sink, n_recent, sel_pages, sel_count, b_max,
+                                       static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
+                           const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
+                           uint64_t seed, uint64_t offset, int32_t* out_tokens,
+                           int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
+  if (n < 0 || k < 0 || vocab <= 0) return S3R_ERR_INVALID_ARG;
+  if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
+  if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n) * (k + 1) * vocab > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
+  size_t need = 0;
+  s3r_spec_sample_workspace_size(n, k, &need);
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < need) return S3R_ERR_WORKSPACE;
+  if (n == 0) return S3R_OK;
+  if (p_logits == nullptr || out_tokens == nullptr || n_accepted == nullptr) return S3R_ERR_INVALID_ARG;
+  if (k > 0 && (q_logits == nullptr || draft_tokens == nullptr)) return S3R_ERR_INVALID_ARG;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  return to_status(launch_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
+                                      static_cast<uint32_t>(offset), reinterpret_cast<float2*>(w + 256),
+                                      out_tokens, n_accepted, reinterpret_cast<int*>(w),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

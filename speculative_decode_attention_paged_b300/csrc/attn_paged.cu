@@ -1,0 +1,713 @@
+// Paged split-KV attention for the three attention forms of an S³R round.
+//
+// What is computed (per the S³R pages):
+//   * dense decode: every step reads the whole history (arXiv abstract;
+//     wispaper.ai "Sparse sampling changes the group, not just the speed");
+//   * sparse draft: the policy reads only its selected pages plus its own
+//     draft tail (wispaper.ai "S3R drafts sparsely and verifies densely");
+//   * verify: T drafted positions attend causally to the complete history
+//     (same section; "Dense verification still pays the full KV-cache bill"),
+//     and the verify attention mass per page feeds the next draft's selection
+//     (rit.work "Как разреженный черновик сохраняет ответы плотной модели").
+//
+// How (B300 design):
+//   * Work unit = one 16-token page of one (sequence, KV head) pair: a 4 KiB K
+//     tile + a 4 KiB V tile, contiguous in the pool.  All pages of all pairs
+//     form one global stream; each warp of a persistent grid (one 8-warp CTA
+//     per SM) takes an equal contiguous share of it, so load balance is exact
+//     whatever the mix of context lengths.  A pair cut by a share boundary
+//     leaves a partial (m, l, O) per side; a small combine kernel merges them
+//     (log-sum-exp merge).  At most two partials per warp are written.
+//   * Each warp runs its own 3-stage TMA pipeline (cp.async.bulk.tensor, one
+//     mbarrier per stage, 128-byte swizzle so ldmatrix reads are
+//     bank-conflict free).  Page ids are fetched 32 at a time, one per lane.
+//   * The G (decode / draft) or T*G (verify) query rows of a pair share every
+//     K/V tile: S = Q K^T and O += P V run on bf16 mma.sync m16n8k16 with the
+//     16 tokens of a page as one n16 / k16 block, fp32 accumulation and an
+//     online softmax in registers (exp2 domain).
+//   * Verify with page mass also stores, per (page, row), the base-2
+//     log-sum-exp of the row's scores over the page; the combine turns it
+//     into the normalised mass sum_r 2^(lse_page,r - LSE_r).
+//   * Data-dependent errors (bad page id, bad length) skip the page and set a
+//     bit in the device error word; every wait is bounded.
+
+#include "attn_paged.cuh"
+#include "s3r_device.cuh"
+
+namespace s3r {
+
+namespace {
+
+constexpr int kStageBytes = 2 * kTileBytes;   // K tile + V tile
+constexpr int kThreads = kAttnWarps * 32;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+struct PairGeom {
+  int np;     // pages in the pair's stream
+  int L;      // ctx_len (dense) or hist_len (sparse / verify)
+  int cnt;    // selected pages (sparse)
+};
+
+// Pages of pair `pair` in the global stream, with its length and selection count.
+__device__ PairGeom pair_geom(const AttnArgs& a, int pair, bool report) {
+  PairGeom g{0, 0, 0};
+  const int s = pair / a.Hkv;
+  const int len = __ldg(a.lens + s);
+  const int cap = a.max_pages * kPage;
+  if (a.mode == kModeDense) {
+    if (len < 0 || len > cap) {
+      if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
+      return g;
+    }
+    g.L = len;
+    g.np = (len + kPage - 1) / kPage;
+  } else if (a.mode == kModeVerify) {
+    if (len < 0 || len + a.T > cap) {
+      if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
+      return g;
+    }
+    g.L = len;
+    g.np = (len + a.T + kPage - 1) / kPage;
+  } else {
+    const int last = len + a.draft_pos;
+    if (len < 0 || last >= cap) {
+      if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
+      return g;
+    }
+    int cnt = __ldg(a.sel_count + pair);
+    if (cnt < 0 || cnt > a.b_max) {
+      if (report) report_error(a.err, S3R_DEVERR_BAD_COUNT);
+      cnt = 0;
+    }
+    g.L = len;
+    g.cnt = cnt;
+    g.np = cnt + (last / kPage - len / kPage + 1);
+  }
+  return g;
+}
+
+struct Entry {
+  int lp;     // logical page
+  int lo;     // first visible token (absolute)
+  int hi;     // one past the last visible token
+  int phys;   // physical page, -1 = nothing to load
+};
+
+// Entry e of pair `pair`'s page stream.
+__device__ Entry pair_entry(const AttnArgs& a, int pair, const PairGeom& g, int e) {
+  Entry r{-1, 0, 0, -1};
+  const int s = pair / a.Hkv;
+  if (a.mode == kModeDense) {
+    r.lp = e;
+    r.lo = e * kPage;
+    r.hi = min(r.lo + kPage, g.L);
+  } else if (a.mode == kModeVerify) {
+    r.lp = e;
+    r.lo = e * kPage;
+    r.hi = min(r.lo + kPage, g.L + a.T);
+  } else if (e < g.cnt) {
+    const int lp = __ldg(a.sel_pages + static_cast<int64_t>(pair) * a.b_max + e);
+    if (lp < 0 || lp >= a.max_pages) {
+      report_error(a.err, S3R_DEVERR_BAD_PAGE);
+      return r;
+    }
+    r.lp = lp;
+    r.lo = lp * kPage;
+    r.hi = min(r.lo + kPage, g.L);
+  } else {
+    r.lp = g.L / kPage + (e - g.cnt);
+    r.lo = max(r.lp * kPage, g.L);
+    r.hi = min(r.lp * kPage + kPage, g.L + a.draft_pos + 1);
+  }
+  if (r.lo < r.hi) {
+    const int phys = __ldg(a.block_table + static_cast<int64_t>(s) * a.max_pages + r.lp);
+    if (phys < 0 || static_cast<int64_t>(phys) >= a.num_phys_pages) {
+      report_error(a.err, S3R_DEVERR_BAD_PAGE);
+    } else {
+      r.phys = phys;
+    }
+  }
+  return r;
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+// Global page index where warp share `gw` starts (shares split N pages evenly).
+__device__ __forceinline__ int64_t share_start(int64_t N, int gw, int tw) {
+  return N * gw / tw;
+}
+
+// The warp share holding global page x (the last share whose start is <= x).
+__device__ __forceinline__ int share_of(int64_t N, int64_t x, int tw) {
+  return static_cast<int>(((x + 1) * tw - 1) / N);
+}
+
+// In-CTA exclusive scan of vals[0..n) in place; vals[n] receives the total.
+__device__ void block_exclusive_scan(int* vals, int n, int* scratch) {
+  const int tid = threadIdx.x;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int b = min(tid * per, n), e = min(b + per, n);
+  int local = 0;
+  for (int i = b; i < e; ++i) local += vals[i];
+  // warp inclusive scan of the thread sums
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kAttnWarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += t;
+    }
+    if (lane < kAttnWarps) scratch[lane] = w;   // inclusive warp totals
+  }
+  __syncthreads();
+  int run = incl - local + (warp > 0 ? scratch[warp - 1] : 0);
+  for (int i = b; i < e; ++i) {
+    const int v = vals[i];
+    vals[i] = run;
+    run += v;
+  }
+  if (tid == kThreads - 1) vals[n] = run;
+  __syncthreads();
+}
+
+// Smem address of the 16-byte chunk holding (token, d0..d0+7) of a swizzled
+// K or V tile: two 64-column halves of 16 rows x 128 B, 128B-swizzled.
+__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int token, int d0) {
+  const int half = d0 >> 6;
+  const int chunk = (d0 & 63) >> 3;
+  return tile + half * kHalfBytes + token * 128 + ((chunk ^ (token & 7)) << 4);
+}
+
+template <int MT, bool MASS>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_partial_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stage_mem = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kAttnStages * kStageBytes);
+  int4* meta = reinterpret_cast<int4*>(bars + kAttnWarps * kAttnStages);   // 2 int4 per stage
+  int* scratch = reinterpret_cast<int*>(meta + 2 * kAttnWarps * kAttnStages);   // 32 ints
+  int* prefix = scratch + 32;                                            // n_chunks + 1
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid < kAttnWarps * kAttnStages) mbar_init(&bars[tid], 1);
+
+  // ---- plan: pages per chunk of 32 pairs, then an exclusive scan
+  for (int c = warp; c < a.n_chunks; c += kAttnWarps) {
+    const int pair = c * kPairChunk + lane;
+    int np = 0;
+    if (pair < a.n_pairs) np = pair_geom(a, pair, blockIdx.x == 0).np;
+    np = warp_sum(np);
+    if (lane == 0) prefix[c] = np;
+  }
+  fence_barrier_init();
+  __syncthreads();
+  block_exclusive_scan(prefix, a.n_chunks, scratch);
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= a.n_chunks; i += kThreads) a.chunk_prefix[i] = prefix[i];
+  }
+
+  const int64_t N = prefix[a.n_chunks];
+  const int tw = a.total_warps;
+  const int gw = blockIdx.x * kAttnWarps + warp;
+  const int64_t x0 = share_start(N, gw, tw);
+  const int64_t x1 = share_start(N, gw + 1, tw);
+  if (x0 >= x1) return;
+
+  uint8_t* my_stages = stage_mem + warp * kAttnStages * kStageBytes;
+  uint64_t* my_bars = bars + warp * kAttnStages;
+  int4* my_meta = meta + 2 * warp * kAttnStages;
+  const uint64_t policy = l2_policy_evict_first();
+
+  // ---- locate the pair holding x0: chunk by binary search, then a warp scan
+  int pr_pair;
+  int64_t pr_pair_start;
+  {
+    int lo = 0, hi = a.n_chunks - 1;   // largest c with prefix[c] <= x0
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= x0) lo = mid; else hi = mid - 1;
+    }
+    const int c = lo;
+    const int pair = c * kPairChunk + lane;
+    const int np = pair < a.n_pairs ? pair_geom(a, pair, false).np : 0;
+    int incl = np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int64_t rel = x0 - prefix[c];
+    const unsigned ball = __ballot_sync(0xffffffffu, incl > rel);
+    const int l = __ffs(ball) - 1;
+    pr_pair = c * kPairChunk + l;
+    pr_pair_start = prefix[c] + __shfl_sync(0xffffffffu, incl - np, l);
+  }
+
+  // ---- producer state (warp-uniform except the per-lane entry cache)
+  PairGeom pr_g = pair_geom(a, pr_pair, false);
+  int pr_e = static_cast<int>(x0 - pr_pair_start);
+  int pr_base = pr_e;
+  Entry cache = pr_base + lane < pr_g.np ? pair_entry(a, pr_pair, pr_g, pr_base + lane)
+                                         : Entry{-1, 0, 0, -1};
+  int64_t pr_x = x0;
+  int64_t pr_k = 0;
+
+  auto produce = [&]() {
+    if (pr_x >= x1) return;
+    if (pr_e >= pr_g.np) {
+      do {
+        ++pr_pair;
+        pr_g = pair_geom(a, pr_pair, false);
+      } while (pr_g.np == 0);
+      pr_e = 0;
+      pr_base = 0;
+      cache = lane < pr_g.np ? pair_entry(a, pr_pair, pr_g, lane) : Entry{-1, 0, 0, -1};
+    } else if (pr_e - pr_base >= 32) {
+      pr_base = pr_e;
+      cache = pr_base + lane < pr_g.np ? pair_entry(a, pr_pair, pr_g, pr_base + lane)
+                                       : Entry{-1, 0, 0, -1};
+    }
+    const int li = pr_e - pr_base;
+    const int lp = __shfl_sync(0xffffffffu, cache.lp, li);
+    const int elo = __shfl_sync(0xffffffffu, cache.lo, li);
+    const int ehi = __shfl_sync(0xffffffffu, cache.hi, li);
+    const int phys = __shfl_sync(0xffffffffu, cache.phys, li);
+    const int st = static_cast<int>(pr_k % kAttnStages);
+    if (lane == 0) {
+      my_meta[2 * st] = make_int4(lp, elo, ehi, phys);
+      my_meta[2 * st + 1] = make_int4(pr_pair, pr_e, pr_g.np, pr_g.L);
+      uint64_t* bar = &my_bars[st];
+      if (phys >= 0) {
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        uint8_t* dst = my_stages + st * kStageBytes;
+        const int y = (pr_pair % a.Hkv) * kPage;
+        fence_proxy_async_smem();
+        tma_load_3d(dst, &kmap, 0, y, phys, bar, policy);
+        tma_load_3d(dst + kHalfBytes, &kmap, 64, y, phys, bar, policy);
+        tma_load_3d(dst + kTileBytes, &vmap, 0, y, phys, bar, policy);
+        tma_load_3d(dst + kTileBytes + kHalfBytes, &vmap, 64, y, phys, bar, policy);
+      } else {
+        mbar_arrive_expect_tx(bar, 0);
+      }
+    }
+    ++pr_e;
+    ++pr_x;
+    ++pr_k;
+  };
+
+  for (int i = 0; i < kAttnStages; ++i) produce();
+
+  // ---- consumer state
+  const int qg = lane >> 2;      // row within an m16 tile (and +8)
+  const int qt = lane & 3;       // column pair selector
+  uint32_t qf[MT][8][4];
+  float o[MT][16][4];
+  float m_r[MT][2], l_r[MT][2];
+  int cur_pair = -1, cur_s = 0, cur_h = 0, cur_L = 0, cur_np = 0, seg_first = 0, seg_last = 0;
+  int seg_index = 0;
+
+  // Per-lane constant parts of the ldmatrix row addresses.
+  const int k_tok = ((lane >> 4) << 3) + (lane & 7);
+  const int k_dsel = (lane >> 3) & 1;
+  const int v_tok = (((lane >> 3) & 1) << 3) + (lane & 7);
+  const int v_dsel = lane >> 4;
+
+  auto q_row_offset = [&](int r) -> int64_t {
+    const int i = r / a.G;
+    const int g = r - i * a.G;
+    return ((static_cast<int64_t>(cur_s) * a.T + i) * a.Hq + cur_h * a.G + g) * kHeadDim;
+  };
+
+  auto begin_pair = [&](int pair, int e_first, int np, int L) {
+    cur_pair = pair;
+    cur_s = pair / a.Hkv;
+    cur_h = pair - cur_s * a.Hkv;
+    cur_L = L;
+    cur_np = np;
+    seg_first = e_first;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      m_r[mt][0] = m_r[mt][1] = kNegInf;
+      l_r[mt][0] = l_r[mt][1] = 0.f;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
+      const int r0 = mt * 16 + qg, r1 = r0 + 8;
+      const bool v0 = r0 < a.R, v1 = r1 < a.R;
+      const uint32_t* q0 = v0 ? reinterpret_cast<const uint32_t*>(a.q + q_row_offset(r0)) : nullptr;
+      const uint32_t* q1 = v1 ? reinterpret_cast<const uint32_t*>(a.q + q_row_offset(r1)) : nullptr;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c0 = (ks * 16 + qt * 2) >> 1, c1 = c0 + 4;   // 32-bit word index
+        qf[mt][ks][0] = v0 ? __ldg(q0 + c0) : 0u;
+        qf[mt][ks][1] = v1 ? __ldg(q1 + c0) : 0u;
+        qf[mt][ks][2] = v0 ? __ldg(q0 + c1) : 0u;
+        qf[mt][ks][3] = v1 ? __ldg(q1 + c1) : 0u;
+      }
+    }
+  };
+
+  auto finish_pair = [&]() {
+    const bool whole = (seg_first == 0) && (seg_last == cur_np - 1);
+    const int slot = gw * 2 + (seg_index == 0 ? 0 : 1);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int r = mt * 16 + qg + hb * 8;
+        const float l = quad_sum(l_r[mt][hb]);
+        const float m = m_r[mt][hb];
+        if (r >= a.R) continue;
+        if (whole) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          float* dst = a.out + q_row_offset(r);
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            *reinterpret_cast<float2*>(dst + n * 8 + qt * 2) =
+                make_float2(o[mt][n][2 * hb] * inv, o[mt][n][2 * hb + 1] * inv);
+          }
+          if (MASS && qt == 0) {
+            a.row_lse[static_cast<int64_t>(cur_pair) * a.R + r] = l > 0.f ? m + fast_log2(l) : kNegInf;
+          }
+        } else {
+          float* po = a.part_o + (static_cast<int64_t>(slot) * a.R + r) * kHeadDim;
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            *reinterpret_cast<float2*>(po + n * 8 + qt * 2) =
+                make_float2(o[mt][n][2 * hb], o[mt][n][2 * hb + 1]);
+          }
+          if (qt == 0) {
+            *reinterpret_cast<float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + r) * 2) =
+                make_float2(m, l);
+          }
+        }
+      }
+    }
+    ++seg_index;
+  };
+
+  bool ok = true;
+  int64_t k_fail = 0;
+  const int64_t n_total = x1 - x0;
+  for (int64_t k = 0; k < n_total; ++k) {
+    const int st = static_cast<int>(k % kAttnStages);
+    const uint32_t parity = static_cast<uint32_t>((k / kAttnStages) & 1);
+    if (!mbar_wait_bounded(&my_bars[st], parity)) {
+      if (lane == 0) report_error(a.err, S3R_DEVERR_TIMEOUT);
+      ok = false;
+      k_fail = k;
+      break;
+    }
+    const int4 m0 = my_meta[2 * st];
+    const int4 m1 = my_meta[2 * st + 1];
+    const int lp = m0.x, elo = m0.y, ehi = m0.z, phys = m0.w;
+    if (m1.x != cur_pair) {
+      if (cur_pair >= 0) finish_pair();
+      begin_pair(m1.x, m1.y, m1.z, m1.w);
+    }
+    seg_last = m1.y;
+
+    if (phys >= 0) {
+      const uint32_t kt = smem_u32(my_stages + st * kStageBytes);
+      const uint32_t vt = kt + kTileBytes;
+      const int page0 = lp * kPage;
+
+      // S = Q K^T for the page's 16 tokens.
+      float sacc[MT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+          sacc[mt][nt][0] = sacc[mt][nt][1] = sacc[mt][nt][2] = sacc[mt][nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(tile_addr(kt, k_tok, ks * 16 + k_dsel * 8), b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_bf16_16816(sacc[mt][0], qf[mt][ks], b0, b1);
+          mma_bf16_16816(sacc[mt][1], qf[mt][ks], b2, b3);
+        }
+      }
+
+      // Mask: page token range, and for verify the causal limit of each row.
+      const bool need_mask = (elo > page0) || (ehi < page0 + kPage) ||
+                             (a.mode == kModeVerify && page0 + kPage - 1 > cur_L);
+      uint32_t pa[MT][4], pl[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        float x[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) x[nt][j] = sacc[mt][nt][j] * a.scale_log2;
+        if (need_mask) {
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const int r = mt * 16 + qg + hb * 8;
+            const int lim = a.mode == kModeVerify ? cur_L + r / a.G : 0x7fffffff;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int t = page0 + nt * 8 + qt * 2 + e;
+                if (t < elo || t >= ehi || t > lim) x[nt][hb * 2 + e] = kNegInf;
+              }
+          }
+        }
+        float alpha[2];
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          float mx = fmaxf(fmaxf(x[0][2 * hb], x[0][2 * hb + 1]), fmaxf(x[1][2 * hb], x[1][2 * hb + 1]));
+          mx = quad_max(mx);
+          const float m_new = fmaxf(m_r[mt][hb], mx);
+          const float m_use = m_new == kNegInf ? 0.f : m_new;
+          alpha[hb] = fast_exp2(m_r[mt][hb] - m_use);
+          float psum = 0.f;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float p = fast_exp2(x[nt][2 * hb + e] - m_use);
+              x[nt][2 * hb + e] = p;
+              psum += p;
+            }
+          l_r[mt][hb] = l_r[mt][hb] * alpha[hb] + psum;
+          m_r[mt][hb] = m_new;
+          if (MASS) {
+            const float ps = quad_sum(psum);
+            const int r = mt * 16 + qg + hb * 8;
+            if (qt == 0 && r < a.R) {
+              a.page_lse[(static_cast<int64_t>(cur_pair) * a.max_pages + lp) * a.R + r] =
+                  ps > 0.f ? m_use + fast_log2(ps) : kNegInf;
+            }
+          }
+        }
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[mt][n][0] *= alpha[0];
+          o[mt][n][1] *= alpha[0];
+          o[mt][n][2] *= alpha[1];
+          o[mt][n][3] *= alpha[1];
+        }
+        // P as bf16 hi + lo parts: P V is then exact to ~2^-16 relative.
+        split_bf16x2(x[0][0], x[0][1], pa[mt][0], pl[mt][0]);
+        split_bf16x2(x[0][2], x[0][3], pa[mt][1], pl[mt][1]);
+        split_bf16x2(x[1][0], x[1][1], pa[mt][2], pl[mt][2]);
+        split_bf16x2(x[1][2], x[1][3], pa[mt][3], pl[mt][3]);
+      }
+
+      // O += P V.
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(tile_addr(vt, v_tok, c * 16 + v_dsel * 8), b0, b1, b2, b3);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          mma_bf16_16816(o[mt][2 * c], pa[mt], b0, b1);
+          mma_bf16_16816(o[mt][2 * c + 1], pa[mt], b2, b3);
+          mma_bf16_16816(o[mt][2 * c], pl[mt], b0, b1);
+          mma_bf16_16816(o[mt][2 * c + 1], pl[mt], b2, b3);
+        }
+      }
+    } else if (MASS && lp >= 0) {
+      // Nothing visible on this page: it holds no mass.
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int r = mt * 16 + qg + hb * 8;
+          if (qt == 0 && r < a.R)
+            a.page_lse[(static_cast<int64_t>(cur_pair) * a.max_pages + lp) * a.R + r] = kNegInf;
+        }
+    }
+    __syncwarp();
+    produce();
+  }
+
+  if (ok) {
+    finish_pair();
+  } else {
+    // Drain whatever copies this warp still has in flight (bounded).
+    for (int64_t k = k_fail; k < pr_k; ++k) {
+      const int st = static_cast<int>(k % kAttnStages);
+      mbar_wait_bounded(&my_bars[st], static_cast<uint32_t>((k / kAttnStages) & 1));
+    }
+  }
+}
+
+// One CTA per (sequence, KV head) pair: merges the partials of a pair cut by
+// warp-share boundaries, writes zero rows for empty pairs and, for verify
+// with page mass, turns the per-page log-sum-exps into normalised mass.
+template <bool MASS>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
+  __shared__ int s_np, s_L;
+  __shared__ long long s_start, s_total;
+  __shared__ float s_lse[S3R_MAX_ROWS_PER_KV_HEAD];
+  const int pair = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const int c = pair / kPairChunk;
+    const int p = c * kPairChunk + tid;
+    const PairGeom g = p < a.n_pairs ? pair_geom(a, p, false) : PairGeom{0, 0, 0};
+    int incl = g.np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += t;
+    }
+    if (p == pair) {
+      s_np = g.np;
+      s_L = g.L;
+      s_start = static_cast<long long>(a.chunk_prefix[c]) + incl - g.np;
+      s_total = a.chunk_prefix[a.n_chunks];
+    }
+  }
+  __syncthreads();
+  const int np = s_np;
+  const int64_t X = s_start, N = s_total;
+  const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
+  auto row_off = [&](int r) -> int64_t {
+    const int i = r / a.G, g = r - (r / a.G) * a.G;
+    return ((static_cast<int64_t>(s) * a.T + i) * a.Hq + h * a.G + g) * kHeadDim;
+  };
+
+  if (np == 0) {
+    for (int idx = tid; idx < a.R * kHeadDim; idx += blockDim.x)
+      a.out[row_off(idx / kHeadDim) + idx % kHeadDim] = 0.f;
+    if (MASS && a.page_mass != nullptr)
+      for (int lp = tid; lp < a.mass_stride; lp += blockDim.x)
+        a.page_mass[static_cast<int64_t>(pair) * a.mass_stride + lp] = 0.f;
+    return;
+  }
+  const int tw = a.total_warps;
+  const int gwa = share_of(N, X, tw);
+  const int gwb = share_of(N, X + np - 1, tw);
+  if (gwa == gwb) {
+    if (!MASS) return;
+    if (tid < a.R) s_lse[tid] = a.row_lse[static_cast<int64_t>(pair) * a.R + tid];
+  } else {
+    for (int r = 0; r < a.R; ++r) {
+      float M = kNegInf;
+      for (int gw = gwa; gw <= gwb; ++gw) {
+        const int64_t st = share_start(N, gw, tw);
+        if (gw > gwa && st == share_start(N, gw + 1, tw)) continue;   // empty share
+        const int slot = gw * 2 + ((gw == gwa && st < X) ? 1 : 0);
+        M = fmaxf(M, a.part_ml[(static_cast<int64_t>(slot) * a.R + r) * 2]);
+      }
+      const float Mu = M == kNegInf ? 0.f : M;
+      float lsum = 0.f, acc = 0.f;
+      for (int gw = gwa; gw <= gwb; ++gw) {
+        const int64_t st = share_start(N, gw, tw);
+        if (gw > gwa && st == share_start(N, gw + 1, tw)) continue;
+        const int slot = gw * 2 + ((gw == gwa && st < X) ? 1 : 0);
+        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + r) * 2);
+        const float w = fast_exp2(ml.x - Mu);
+        lsum += ml.y * w;
+        acc += a.part_o[(static_cast<int64_t>(slot) * a.R + r) * kHeadDim + tid] * w;
+      }
+      a.out[row_off(r) + tid] = lsum > 0.f ? acc / lsum : 0.f;
+      if (MASS && tid == 0) s_lse[r] = lsum > 0.f ? M + fast_log2(lsum) : kNegInf;
+    }
+  }
+  if (!MASS || a.page_mass == nullptr) return;
+  __syncthreads();
+  for (int lp = tid; lp < a.mass_stride; lp += blockDim.x) {
+    float mass = 0.f;
+    if (lp < np) {
+      const float* pl = a.page_lse + (static_cast<int64_t>(pair) * a.max_pages + lp) * a.R;
+      for (int r = 0; r < a.R; ++r) {
+        const float v = pl[r];
+        if (v != kNegInf && s_lse[r] != kNegInf) mass += fast_exp2(v - s_lse[r]);
+      }
+    }
+    a.page_mass[static_cast<int64_t>(pair) * a.mass_stride + lp] = mass;
+  }
+}
+
+template <int MT, bool MASS>
+cudaError_t launch_variant(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
+                           int grid, cudaStream_t stream) {
+  const size_t smem = attn_smem_bytes(a.n_chunks);
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<MT, MASS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  attn_partial_kernel<MT, MASS><<<grid, kThreads, smem, stream>>>(kmap, vmap, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_combine_kernel<MASS><<<a.n_pairs, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_smem_bytes(int n_chunks) {
+  return 1024 + static_cast<size_t>(kAttnWarps) * kAttnStages * kStageBytes +
+         static_cast<size_t>(kAttnWarps) * kAttnStages * (8 + 32) + 32 * 4 +
+         static_cast<size_t>(n_chunks + 1) * 4;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+AttnWorkspaceLayout attn_workspace_layout(int n_pairs, int rows, int max_pages, int total_warps,
+                                          bool with_mass) {
+  AttnWorkspaceLayout L{};
+  const int n_chunks = (n_pairs + kPairChunk - 1) / kPairChunk;
+  size_t off = 0;
+  L.err_off = off;
+  off += 256;
+  L.prefix_off = off;
+  off = align256(off + static_cast<size_t>(n_chunks + 1) * 4);
+  L.part_o_off = off;
+  off = align256(off + static_cast<size_t>(2) * total_warps * rows * kHeadDim * 4);
+  L.part_ml_off = off;
+  off = align256(off + static_cast<size_t>(2) * total_warps * rows * 2 * 4);
+  L.row_lse_off = off;
+  if (with_mass) off = align256(off + static_cast<size_t>(n_pairs) * rows * 4);
+  L.page_lse_off = off;
+  if (with_mass) off = align256(off + static_cast<size_t>(n_pairs) * max_pages * rows * 4);
+  L.total = off;
+  return L;
+}
+
+cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
+                             int grid, cudaStream_t stream) {
+  const bool mass = a.mode == kModeVerify && a.page_mass != nullptr;
+  if (a.R <= 16) {
+    return mass ? launch_variant<1, true>(kmap, vmap, a, grid, stream)
+                : launch_variant<1, false>(kmap, vmap, a, grid, stream);
+  }
+  return mass ? launch_variant<2, true>(kmap, vmap, a, grid, stream)
+              : launch_variant<2, false>(kmap, vmap, a, grid, stream);
+}
+
+}  // namespace s3r

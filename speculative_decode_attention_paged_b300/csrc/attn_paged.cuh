@@ -1,0 +1,63 @@
+// Paged split-KV attention engine shared by the three attention forms of an
+// S³R round: dense decode, budgeted sparse draft, dense causal verify (+ page
+// mass).  Host-visible launch interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace s3r {
+
+enum AttnMode : int { kModeDense = 0, kModeSparse = 1, kModeVerify = 2 };
+
+constexpr int kAttnWarps = 8;       // warps per CTA, each an independent worker
+constexpr int kAttnStages = 3;      // TMA stages per warp (one (page, KV head) K+V tile each)
+constexpr int kPairChunk = 32;      // (sequence, KV head) pairs per prefix-sum chunk
+constexpr int kMaxPairs = 262144;   // chunk prefix must fit in shared memory
+
+struct AttnArgs {
+  int mode;
+  int S, Hq, Hkv, G, T, R;          // R = T * G query rows per (sequence, KV head) pair
+  int max_pages;
+  int64_t num_phys_pages;
+  const int32_t* block_table;
+  const int32_t* lens;              // ctx_lens (dense) or hist_lens (sparse, verify)
+  int draft_pos;
+  const int32_t* sel_pages;
+  const int32_t* sel_count;
+  int b_max;
+  const __nv_bfloat16* q;
+  float* out;                       // fp32 attention output
+  float scale_log2;                 // sm_scale * log2(e)
+  float* page_mass;                 // verify only, may be null
+  int mass_stride;
+  // workspace views
+  int* err;
+  int* chunk_prefix;                // [n_chunks + 1]
+  float* part_o;                    // [2 * total_warps][R][128]
+  float* part_ml;                   // [2 * total_warps][R][2]
+  float* row_lse;                   // [n_pairs][R]             (page mass only)
+  float* page_lse;                  // [n_pairs][max_pages][R]  (page mass only)
+  int total_warps;
+  int n_pairs;
+  int n_chunks;
+};
+
+struct AttnWorkspaceLayout {
+  size_t err_off, prefix_off, part_o_off, part_ml_off, row_lse_off, page_lse_off, total;
+};
+
+// Byte layout of the attention workspace for the given geometry.
+AttnWorkspaceLayout attn_workspace_layout(int n_pairs, int rows, int max_pages, int total_warps,
+                                          bool with_mass);
+
+size_t attn_smem_bytes(int n_chunks);
+
+// Enqueue the partial and combine kernels.  `a` must be fully populated.
+cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
+                             int grid, cudaStream_t stream);
+
+}  // namespace s3r

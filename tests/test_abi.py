@@ -1,0 +1,79 @@
+"""The C-ABI library loads, exports every entry point include/s3r.h declares,
+and rejects bad arguments on the host before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decode_attention_paged_b300 as s3r
+from speculative_decode_attention_paged_b300 import build as s3r_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "s3r.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"S3R_API\s+[^;(]*?\b(s3r_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    s3r_build.build()
+    return s3r.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for want in ("s3r_dense_decode_attn", "s3r_sparse_draft_attn", "s3r_verify_attn",
+                 "s3r_select_draft_pages", "s3r_spec_sample"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_host_only_queries(lib):
+    assert s3r.s3r_version().startswith("s3r-b300")
+    assert lib.s3r_status_string(0) == b"S3R_OK"
+    assert lib.s3r_status_string(4) == b"S3R_ERR_WORKSPACE"
+    assert s3r.s3r_select_workspace_size() == 256
+    assert s3r.s3r_spec_sample_workspace_size(2048, 8) >= 256 + 2048 * 17 * 8
+    with pytest.raises(s3r.S3RError):
+        s3r.s3r_spec_sample_workspace_size(4, 65)
+
+
+def _kv(**over):
+    f = dict(k_pool=None, v_pool=None, num_phys_pages=10, block_table=None, max_pages_per_seq=4,
+             num_seqs=0, num_q_heads=16, num_kv_heads=8, head_dim=128, page_size=16)
+    f.update(over)
+    return s3r._PagedKV(**f)
+
+
+def test_argument_validation_on_host(lib):
+    size = ctypes.c_size_t(0)
+    # head_dim / page size the kernels do not implement
+    assert lib.s3r_attn_workspace_size(ctypes.byref(_kv(head_dim=64)), 1, ctypes.byref(size)) == 2
+    assert lib.s3r_attn_workspace_size(ctypes.byref(_kv(page_size=32)), 1, ctypes.byref(size)) == 2
+    # q heads not a multiple of KV heads
+    assert lib.s3r_attn_workspace_size(ctypes.byref(_kv(num_q_heads=12)), 1, ctypes.byref(size)) == 1
+    # rows per KV head above the limit (G = 16, T = 4)
+    assert lib.s3r_attn_workspace_size(ctypes.byref(_kv(num_q_heads=128)), 4, ctypes.byref(size)) == 2
+    # attention with a missing workspace
+    kv = _kv()
+    assert lib.s3r_dense_decode_attn(ctypes.byref(kv), None, None, None, ctypes.c_float(1.0), None, 0, None) == 4
+    assert lib.s3r_verify_attn(ctypes.byref(kv), None, 0, None, None, None, 0, ctypes.c_float(1.0), None, 0,
+                               None) == 1
+    # selection: bad geometry, bad budget, b_max below the budget of mass_stride pages
+    assert lib.s3r_select_draft_pages(None, None, 1, 0, 8, ctypes.c_double(0.05), 1, 4, None, None, 8,
+                                      None, 0, None) == 1
+    assert lib.s3r_select_draft_pages(None, None, 1, 8, 8, ctypes.c_double(1.5), 1, 4, None, None, 8,
+                                      None, 0, None) == 1
+    # spec sample: k above the limit, empty vocabulary, offset beyond 32 bits
+    assert lib.s3r_spec_sample(None, None, None, 1, 65, 10, 0, 0, None, None, None, 0, None) == 2
+    assert lib.s3r_spec_sample(None, None, None, 1, 4, 0, 0, 0, None, None, None, 0, None) == 1
+    assert lib.s3r_spec_sample(None, None, None, 1, 4, 10, 0, 1 << 32, None, None, None, 0, None) == 1

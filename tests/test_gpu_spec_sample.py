@@ -1,0 +1,139 @@
+"""GPU parity of exact speculative sampling against the oracle.
+
+Given identical fp32 logits and identical Philox uniforms, accept/reject
+decisions and sampled tokens must match bit for bit, except floating-point
+ties, which are counted and bounded:
+  * a ratio tie: |u - p_i(x_i)/q_i(x_i)| <= 1e-6;
+  * a resample tie: the GPU token is still a valid inverse-CDF answer for the
+    oracle's fp64 CDF C of the row within 2e-6 * Z:
+    C[y-1] <= u*Z + 2e-6*Z and C[y] >= u*Z - 2e-6*Z.
+The exactness theorem itself is checked on the GPU too (chi-square of the
+first emitted token against p_1 over 10^6 sequences)."""
+
+import numpy as np
+import pytest
+import torch
+from scipy import special, stats
+
+import oracle
+import speculative_decode_attention_paged_b300 as s3r
+from workloads import SAMPLER_CONFIGS, make_spec_inputs
+from helpers import host
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+RATIO_TIE = 1e-6
+CDF_TIE = 2e-6
+
+
+def _gpu(inp, seed, offset=0):
+    N, k1, V = inp.p_logits.shape
+    k = k1 - 1
+    ws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(N, k))
+    out = torch.full((N, k + 1), 77, dtype=torch.int32, device=DEV)
+    nacc = torch.full((N,), 77, dtype=torch.int32, device=DEV)
+    s3r.s3r_spec_sample(inp.p_logits, inp.q_logits, inp.draft_tokens, seed, offset, out, nacc, ws)
+    ws.check()
+    return host(out), host(nacc)
+
+
+def compare(p_logits, q_logits, drafts, seed, offset, out_g, nacc_g, max_tie_frac=0.01, seq_ids=None):
+    """Oracle on the same host arrays; returns (ratio_ties, cdf_ties)."""
+    out_o, nacc_o, det = oracle.spec_sample(p_logits, q_logits, drafts, seed, offset, seq_ids=seq_ids)
+    N, k = drafts.shape
+    ratio_ties = cdf_ties = 0
+    for n in range(N):
+        if nacc_g[n] != nacc_o[n]:
+            i = min(nacc_g[n], nacc_o[n])     # first position where the decisions differ
+            gap = abs(det["u_accept"][n, i] - det["ratio"][n, i])
+            assert gap <= RATIO_TIE, f"seq {n}: accept decision differs at {i}, |u - ratio| = {gap:.3e}"
+            ratio_ties += 1
+            continue
+        assert np.array_equal(out_g[n, : nacc_g[n]], out_o[n, : nacc_o[n]])
+        assert np.all(out_g[n, nacc_g[n] + 1:] == -1)
+        yg, yo = int(out_g[n, nacc_g[n]]), int(out_o[n, nacc_o[n]])
+        if yg != yo:
+            a = int(nacc_o[n])
+            if a < k:
+                row = oracle.residual_row(p_logits[n, a], q_logits[n, a])
+            else:
+                row = np.exp(p_logits[n, k].astype(np.float64) - p_logits[n, k].max())
+                row /= row.sum()
+            C = np.cumsum(row)
+            Z = C[-1]
+            t = det["u_resample"][n] * Z
+            lo = C[yg - 1] if yg > 0 else 0.0
+            assert 0 <= yg < len(row) and row[yg] > 0, f"seq {n}: token {yg} has zero probability"
+            assert lo <= t + CDF_TIE * Z and C[yg] >= t - CDF_TIE * Z, f"seq {n}: token {yg} vs {yo}"
+            cdf_ties += 1
+    assert ratio_ties + cdf_ties <= max(2, max_tie_frac * N), (ratio_ties, cdf_ties)
+    return ratio_ties, cdf_ties
+
+
+def test_config1_tiny_full():
+    cfg = SAMPLER_CONFIGS[1]
+    inp = make_spec_inputs(cfg.num_seqs, cfg.k, cfg.vocab, cfg.p_sigma, cfg.q_sigmas[0], cfg.seed, device=DEV)
+    out, nacc = _gpu(inp, cfg.philox_seed)
+    compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), cfg.philox_seed, 0, out, nacc)
+
+
+@pytest.mark.parametrize("sigma", [0.3, 1.0, 3.0])
+def test_qwen_vocab_many_sequences(sigma):
+    inp = make_spec_inputs(256, 8, 151936, 3.0, sigma, seed=int(sigma * 10), device=DEV)
+    out, nacc = _gpu(inp, seed=12345, offset=7)
+    compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), 12345, 7, out, nacc)
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 5, 127, 1000, 4099])
+def test_odd_vocab_sizes(V):
+    inp = make_spec_inputs(64, 4, V, 2.0, 1.0, seed=V, device=DEV)
+    out, nacc = _gpu(inp, seed=99)
+    compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), 99, 0, out, nacc)
+
+
+def test_q_equals_p_accepts_everything():
+    inp = make_spec_inputs(128, 6, 5000, 3.0, 0.0, seed=3, device=DEV)
+    out, nacc = _gpu(inp, seed=5)
+    assert np.all(nacc == 6)
+    compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), 5, 0, out, nacc)
+
+
+def test_k_zero_samples_bonus_only():
+    inp = make_spec_inputs(32, 0, 1000, 3.0, 1.0, seed=4, device=DEV)
+    out, nacc = _gpu(inp, seed=6)
+    assert np.all(nacc == 0)
+    compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), 6, 0, out, nacc)
+
+
+def test_config4_rollout_scale_sampled():
+    cfg = SAMPLER_CONFIGS[4]
+    for sigma in cfg.q_sigmas:
+        inp = make_spec_inputs(cfg.num_seqs, cfg.k, cfg.vocab, cfg.p_sigma, sigma, cfg.seed, device=DEV)
+        out, nacc = _gpu(inp, cfg.philox_seed)
+        # acceptance is what the noise level implies (~95% / ~80% per position)
+        rate = (nacc[:, None] > np.arange(cfg.k)[None, :]).sum() / max(1, (np.minimum(nacc + 1, cfg.k)).sum())
+        assert 0.5 < rate < 1.0
+        rng = np.random.default_rng(int(sigma * 100))
+        seqs = np.sort(rng.choice(cfg.num_seqs, size=48, replace=False))
+        compare(host(inp.p_logits[seqs]), host(inp.q_logits[seqs]), host(inp.draft_tokens[seqs]),
+                cfg.philox_seed, 0, out[seqs], nacc[seqs], max_tie_frac=0.05, seq_ids=seqs)
+
+
+def test_exactness_theorem_on_gpu():
+    """First emitted token ~ p_1 over 10^6 sequences (chi-square)."""
+    N, k, V = 1_000_000, 3, 12
+    rng = np.random.default_rng(9)
+    p_row = rng.normal(0, 1.5, size=(k + 1, V)).astype(np.float32)
+    q_row = (p_row[:k] + rng.normal(0, 1.0, size=(k, V))).astype(np.float32)
+    p = torch.from_numpy(p_row).to(DEV).expand(N, k + 1, V).contiguous()
+    q = torch.from_numpy(q_row).to(DEV).expand(N, k, V).contiguous()
+    qprob = special.softmax(q_row.astype(np.float64), axis=-1)
+    x = np.stack([rng.choice(V, size=N, p=qprob[i]) for i in range(k)], axis=1).astype(np.int32)
+    inp = type("I", (), {})()
+    inp.p_logits, inp.q_logits, inp.draft_tokens = p, q, torch.from_numpy(x).to(DEV)
+    out, nacc = _gpu(inp, seed=2024)
+    pprob = special.softmax(p_row.astype(np.float64), axis=-1)
+    for j in range(k + 1):
+        have = nacc >= j
+        counts = np.bincount(out[have, j], minlength=V)
+        assert stats.chisquare(counts, pprob[j] * have.sum()).pvalue > 1e-3
