@@ -1,0 +1,581 @@
+"""Benchmark of the S³R paged decode-attention hot path on one B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl s3r|reference]
+
+One step is one pass of the whole hot path over one batch of synthetic input
+shaped like the Qwen3-1.7B rollout workload (one attention layer, 256
+sequences, histories U{4096..16384}, 16 query / 8 KV heads, head_dim 128,
+16-token bf16 pages in a randomly permuted pool, k = 4, budget 0.05, Qwen3
+vocabulary 151936 for the sampler):
+
+  1. k dense decode steps (the autoregressive baseline, positions L .. L+k-1);
+  2. verification of the k-token block with page mass;
+  3. draft-page selection from that mass (history L + k);
+  4. k sparse draft steps of the next round over the selected pages;
+  5. exact speculative sampling of the 256 drafted blocks.
+
+`value` is the algorithmic HBM throughput of the whole step in GB/s (KV bytes
+of every attention call + queries/outputs + page mass + selection + logits,
+section "Bytes" of the design notes) divided by the device time of the step;
+the per-phase split, the draft+verify attention tokens/s, the dense tokens/s
+and the effective tokens/s at the measured acceptance are extra keys.  The
+reference arm (--impl reference) times the fp64 CPU oracle on a bounded sample
+of the same workload.
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import ATTN_CONFIGS, SAMPLER_CONFIGS, make_paged_kv, make_queries, make_spec_inputs  # noqa: E402
+
+METRIC = "KV GB/s (% of 8 TB/s) and draft+verify attention tokens/s at 1 B300"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+KV_TOKEN_BYTES_PER_HEAD = 2 * 128 * 2          # K + V rows of one token of one KV head, bf16
+SMI_FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+def selection_budget_pages(P, budget, n_sink=1, n_recent=4):
+    mand = min(n_sink, P) + (P - max(max(P - n_recent, 0), min(n_sink, P)))
+    return min(P, max(math.ceil(budget * P - 1e-9), mand))
+
+
+# ---------------------------------------------------------------- workload
+
+class Workload:
+    """Device-resident inputs of one step (built once, reused every step)."""
+
+    def __init__(self, device, attn_cfg=2, sampler_cfg=2, num_seqs=None):
+        self.cfg = ATTN_CONFIGS[attn_cfg]
+        self.scfg = SAMPLER_CONFIGS[sampler_cfg]
+        if num_seqs is not None:
+            import dataclasses
+            self.cfg = dataclasses.replace(self.cfg, num_seqs=int(num_seqs))
+            self.scfg = dataclasses.replace(self.scfg, num_seqs=int(num_seqs))
+        c = self.cfg
+        self.k = c.k
+        self.budget = c.budgets[0]
+        # capacity for the verified block and the next round's draft tail
+        self.kv = make_paged_kv(c.num_seqs, c.q_heads, c.kv_heads, 2 * c.k, seed=c.seed, device=device,
+                                hist_min=c.hist_min, hist_max=c.hist_max,
+                                heavy_per_head=c.heavy_per_head, heavy_score=c.heavy_score)
+        kv = self.kv
+        S, Hq, Hkv, k = kv.num_seqs, kv.q_heads, kv.kv_heads, self.k
+        self.S, self.Hq, self.Hkv = S, Hq, Hkv
+        self.q_verify = make_queries(kv, 1000, rows=k)
+        self.q_dense = [make_queries(kv, 1100 + j) for j in range(k)]
+        self.q_draft = [make_queries(kv, 1200 + j) for j in range(k)]
+        self.ctx_dense = [(kv.hist_lens + j + 1).to(torch.int32) for j in range(k)]
+        self.sel_lens = (kv.hist_lens + k).to(torch.int32)
+        self.mass_stride = kv.max_pages
+        self.b_max = selection_budget_pages(self.mass_stride, self.budget)
+        sc = self.scfg
+        self.spec = make_spec_inputs(sc.num_seqs, sc.k, sc.vocab, sc.p_sigma, sc.q_sigmas[0], sc.seed,
+                                     device=device)
+        self.N, self.V = sc.num_seqs, sc.vocab
+        # outputs
+        f32 = dict(dtype=torch.float32, device=device)
+        self.out_dense = [torch.empty(q.shape, **f32) for q in self.q_dense]
+        self.out_verify = torch.empty(self.q_verify.shape, **f32)
+        self.out_draft = [torch.empty(q.shape, **f32) for q in self.q_draft]
+        self.mass = torch.empty((S, Hkv, self.mass_stride), **f32)
+        self.sel = torch.empty((S, Hkv, self.b_max), dtype=torch.int32, device=device)
+        self.cnt = torch.empty((S, Hkv), dtype=torch.int32, device=device)
+        self.out_tokens = torch.empty((self.N, sc.k + 1), dtype=torch.int32, device=device)
+        self.n_acc = torch.empty((self.N,), dtype=torch.int32, device=device)
+
+    # ---- algorithmic bytes (per call), used for value and the roofline
+    def dense_bytes(self, j):
+        L = self.kv.hist_lens.double()
+        kv_bytes = float((L + j + 1).sum()) * self.Hkv * KV_TOKEN_BYTES_PER_HEAD
+        return kv_bytes + self.S * self.Hq * 128 * (2 + 4)
+
+    def verify_bytes(self):
+        L = self.kv.hist_lens.double()
+        kv_bytes = float((L + self.k).sum()) * self.Hkv * KV_TOKEN_BYTES_PER_HEAD
+        return kv_bytes + self.S * self.k * self.Hq * 128 * (2 + 4) + self.S * self.Hkv * self.mass_stride * 4
+
+    def select_bytes(self):
+        return self.S * self.Hkv * (self.mass_stride + self.b_max + 1) * 4
+
+    def draft_tokens_visible(self, j):
+        """Tokens each (sequence, KV head) of draft step j reads (host count
+        from the selection, which is the same every step)."""
+        sel = self.sel.cpu().numpy()
+        cnt = self.cnt.cpu().numpy()
+        Lsel = self.sel_lens.cpu().numpy().astype(np.int64)
+        total = 0
+        for s in range(self.S):
+            L = int(Lsel[s])
+            for h in range(self.Hkv):
+                pages = sel[s, h, : cnt[s, h]].astype(np.int64)
+                total += int(np.minimum(pages * 16 + 16, L).sum() - np.minimum(pages * 16, L).sum())
+            total += self.Hkv * (j + 1)
+        return total
+
+    def draft_bytes(self, j):
+        return (self._draft_tok[j] * KV_TOKEN_BYTES_PER_HEAD + self.S * self.Hq * 128 * (2 + 4)
+                + self.S * self.Hkv * (self.b_max + 1) * 4)
+
+    def sample_bytes(self):
+        k = self.scfg.k
+        return self.N * (2 * k + 1) * self.V * 4 + self.N * (k + (k + 1) + 1) * 4
+
+    def finalize_bytes(self):
+        self._draft_tok = [self.draft_tokens_visible(j) for j in range(self.k)]
+        self.bytes = {
+            "dense": [self.dense_bytes(j) for j in range(self.k)],
+            "verify": self.verify_bytes(),
+            "select": self.select_bytes(),
+            "draft": [self.draft_bytes(j) for j in range(self.k)],
+            "sample": self.sample_bytes(),
+        }
+        b = self.bytes
+        self.step_bytes = sum(b["dense"]) + b["verify"] + b["select"] + sum(b["draft"]) + b["sample"]
+
+
+class Runner:
+    """Issues one step through the C-ABI binding, with events between phases."""
+
+    PHASES = ("dense", "verify", "select", "draft", "sample")
+
+    def __init__(self, w: Workload):
+        import speculative_decode_attention_paged_b300 as s3r
+        self.s3r = s3r
+        self.w = w
+        self.desc = s3r.PagedKVDesc(w.kv.k_pool, w.kv.v_pool, w.kv.block_table, w.kv.q_heads)
+        dev = w.kv.k_pool.device
+        self.ws = s3r.Workspace(s3r.s3r_attn_workspace_size(self.desc, w.k), device=dev)
+        self.sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(w.N, w.scfg.k), device=dev)
+        self.launches_per_step = 2 * w.k + 2 + 1 + 2 * w.k + 2
+
+    def step(self, ev=None):
+        """ev: list of 2k+4 events recorded at the phase boundaries, or None."""
+        s3r, w = self.s3r, self.w
+        i = 0
+
+        def mark():
+            nonlocal i
+            if ev is not None:
+                ev[i].record()
+            i += 1
+
+        mark()
+        for j in range(w.k):
+            s3r.s3r_dense_decode_attn(self.desc, w.ctx_dense[j], w.q_dense[j], w.out_dense[j], 1.0, self.ws)
+            mark()
+        s3r.s3r_verify_attn(self.desc, w.kv.hist_lens, w.q_verify, w.out_verify, 1.0, self.ws, page_mass=w.mass)
+        mark()
+        s3r.s3r_select_draft_pages(w.mass, w.sel_lens, w.budget, w.sel, w.cnt, self.ws)
+        mark()
+        for j in range(w.k):
+            s3r.s3r_sparse_draft_attn(self.desc, w.sel_lens, j, w.sel, w.cnt, w.q_draft[j], w.out_draft[j], 1.0,
+                                      self.ws)
+            mark()
+        s3r.s3r_spec_sample(w.spec.p_logits, w.spec.q_logits, w.spec.draft_tokens, w.scfg.philox_seed, 0,
+                            w.out_tokens, w.n_acc, self.sws)
+        mark()
+
+    def n_events(self):
+        return 2 * self.w.k + 4
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"s3r_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and parts[0] != self.uuid:
+                    continue
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+
+_ORACLE_INPUTS = {}
+
+
+def oracle_sample(seconds, seed=0):
+    """Run the fp64 oracle over whole sequences of a host-sized slice of the
+    same workload until `seconds` of CPU work are spent; returns (bytes, time,
+    description).  The slice is regenerated on the CPU with the same recipe
+    (same shapes and distributions, fewer sequences)."""
+    import oracle
+    from workloads import bf16_to_bits
+
+    c = ATTN_CONFIGS[2]
+    sc = SAMPLER_CONFIGS[2]
+    n_seqs = 8
+    if seed not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS.clear()
+        kv = make_paged_kv(n_seqs, c.q_heads, c.kv_heads, 2 * c.k, seed=c.seed + 100 + seed, device="cpu",
+                           hist_min=c.hist_min, hist_max=c.hist_max)
+        spec = make_spec_inputs(n_seqs, sc.k, sc.vocab, sc.p_sigma, sc.q_sigmas[0], sc.seed + 100 + seed)
+        _ORACLE_INPUTS[seed] = (
+            bf16_to_bits(kv.k_pool), bf16_to_bits(kv.v_pool), kv.block_table.numpy(),
+            kv.hist_lens.numpy().astype(np.int64), bf16_to_bits(make_queries(kv, 1000, rows=c.k)),
+            bf16_to_bits(make_queries(kv, 1100)), spec.p_logits.numpy(), spec.q_logits.numpy(),
+            spec.draft_tokens.numpy())
+    kp, vp, bt, L, qv, qd, p_l, q_l, x_l = _ORACLE_INPUTS[seed]
+    k = c.k
+    Hkv, Hq = c.kv_heads, c.q_heads
+    done_bytes = 0.0
+    t0 = time.perf_counter()
+    seqs_done = 0
+    for s in range(n_seqs):
+        one = [s]
+        for j in range(k):
+            oracle.dense_decode_attn(qd, kp, vp, bt, L + j + 1, 1.0, seqs=one)
+            done_bytes += (L[s] + j + 1) * Hkv * KV_TOKEN_BYTES_PER_HEAD + Hq * 128 * 6
+        _, mass = oracle.verify_attn(qv, kp, vp, bt, L, 1.0, seqs=one, mass_pages=bt.shape[1])
+        done_bytes += (L[s] + k) * Hkv * KV_TOKEN_BYTES_PER_HEAD + k * Hq * 128 * 6 + Hkv * bt.shape[1] * 4
+        sel, cnt = oracle.select_draft_pages(mass, L[one] + k, c.budgets[0], 1, 4)
+        done_bytes += Hkv * (bt.shape[1] + sel.shape[-1]) * 4
+        sel_full = np.full((n_seqs, Hkv, sel.shape[-1]), -1, dtype=np.int64)
+        cnt_full = np.zeros((n_seqs, Hkv), dtype=np.int64)
+        sel_full[s], cnt_full[s] = sel[0], cnt[0]
+        for j in range(k):
+            oracle.sparse_draft_attn(qd, kp, vp, bt, L + k, j, sel_full, cnt_full, 1.0, seqs=one)
+            vis = 0
+            for h in range(Hkv):
+                pg = sel[0, h, : cnt[0, h]]
+                vis += int(np.minimum(pg * 16 + 16, L[s] + k).sum() - np.minimum(pg * 16, L[s] + k).sum()) + j + 1
+            done_bytes += vis * KV_TOKEN_BYTES_PER_HEAD + Hq * 128 * 6
+        oracle.spec_sample(p_l[one], q_l[one], x_l[one], sc.philox_seed, 0, seq_ids=one)
+        done_bytes += (2 * sc.k + 1) * sc.vocab * 4
+        seqs_done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    desc = (f"{seqs_done} whole sequence(s) of the 256-sequence step (same recipe, histories U{{4096..16384}}): "
+            f"{k} dense decode steps, verify+mass, select, {k} sparse drafts, spec sample over V={sc.vocab}; "
+            f"fp64 NumPy oracle")
+    return done_bytes, dt, desc
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max([d.get("num_threads", 1) for d in info] + [1])
+    except Exception:
+        return 1
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    per_step = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
+    for _ in range(args.warmup):
+        oracle_sample(per_step / 4)
+    total_b, total_t, desc = 0.0, 0.0, ""
+    for i in range(args.steps):
+        b, t, desc = oracle_sample(per_step)
+        total_b += b
+        total_t += t
+    value = total_b / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "qwen3-1.7b-geom 1 layer, 256 seqs x U{4096..16384}, 16/8 heads, d=128, k=4, "
+                               "budget 0.05, vocab 151936 (bounded sample per step)",
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_s3r(args, world, rank, local):
+    import speculative_decode_attention_paged_b300 as s3r
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    s3r.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = Workload(dev, num_seqs=args.seqs)
+    r = Runner(w)
+    r.step()
+    torch.cuda.synchronize()
+    w.finalize_bytes()
+    r.ws.check()
+    r.sws.check()
+
+    for _ in range(args.warmup):
+        r.step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    nev = r.n_events()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) is not None else None
+    clocks = ClockSampler(uuid) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for i in range(K):
+        r.step(evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clock_info = clocks.stop() if clocks else None
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms_max = allreduce_max(total_ms, world)
+    r.ws.check()
+    r.sws.check()
+
+    # per-phase durations (ms), averaged over the K steps
+    k = w.k
+    ph = {"dense": [], "verify": [], "select": [], "draft": [], "sample": []}
+    dense_launch_ms = []
+    for e in evs:
+        d = [e[j].elapsed_time(e[j + 1]) for j in range(nev - 1)]
+        ph["dense"].append(sum(d[0:k]))
+        dense_launch_ms.extend(d[0:k])
+        ph["verify"].append(d[k])
+        ph["select"].append(d[k + 1])
+        ph["draft"].append(sum(d[k + 2: 2 * k + 2]))
+        ph["sample"].append(d[2 * k + 2])
+    pm = {key: statistics.mean(v) for key, v in ph.items()}
+
+    ms_per_step = total_ms_max / K
+    value = world * w.step_bytes / (ms_per_step * 1e-3) / 1e9
+    b = w.bytes
+    dense_avg_bytes = sum(b["dense"]) / k
+    dense_launch = statistics.mean(dense_launch_ms)
+    achieved = dense_avg_bytes / (dense_launch * 1e-3) / 1e9
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = float(peaks.get("hbm_gbs", 6400.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    nacc = w.n_acc.cpu().numpy()
+    mean_emitted = float((nacc + 1).mean())
+    t_round = (pm["verify"] + pm["select"] + pm["draft"]) * 1e-3
+    dv_tokens = w.S * k / t_round
+    dense_tokens = w.S * k / (pm["dense"] * 1e-3)
+    eff_tokens = w.S * mean_emitted / (t_round + pm["sample"] * 1e-3)
+
+    def gbs(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9
+
+    phases = {
+        "dense_x%d" % k: {"ms": pm["dense"], "gb": sum(b["dense"]) / 1e9, "gbs": gbs(sum(b["dense"]), pm["dense"])},
+        "verify": {"ms": pm["verify"], "gb": b["verify"] / 1e9, "gbs": gbs(b["verify"], pm["verify"])},
+        "select": {"ms": pm["select"], "gb": b["select"] / 1e9, "gbs": gbs(b["select"], pm["select"])},
+        "draft_x%d" % k: {"ms": pm["draft"], "gb": sum(b["draft"]) / 1e9, "gbs": gbs(sum(b["draft"]), pm["draft"])},
+        "spec_sample": {"ms": pm["sample"], "gb": b["sample"] / 1e9, "gbs": gbs(b["sample"], pm["sample"])},
+    }
+
+    # ---- end to end: host (pinned) inputs -> device -> C-ABI calls -> host results
+    e2e = run_e2e(w, r, max(3, min(K, 5)), world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"qwen3-1.7b-geom 1 layer: {w.S} seqs x U{{4096..16384}}, 16 q / 8 kv heads, d=128, "
+                               "16-token bf16 pages (permuted pool), k=4, budget 0.05; sampler 256 x k=4 x "
+                               "V=151936 fp32, sigma=1.0",
+                   "step": "4 dense decode + verify(page mass) + select + 4 sparse drafts + spec sample",
+                   "l2": "inputs larger than L2 (step reads %.1f GB vs 126 MB L2)" % (w.step_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "1 gpu"},
+        "kv_pct_of_8tbs": 100.0 * value / NOMINAL_HBM_GBS,
+        "pct_of_measured_hbm": 100.0 * value / peak,
+        "draft_verify_attn_tokens_per_s": dv_tokens * world,
+        "dense_decode_tokens_per_s": dense_tokens * world,
+        "effective_tokens_per_s": eff_tokens * world,
+        "mean_accepted_plus_one": mean_emitted,
+        "round_vs_dense_speedup": pm["dense"] / (pm["verify"] + pm["select"] + pm["draft"] + pm["sample"]),
+        "phases": phases,
+        "roofline": {"kernel": "attn_partial_kernel (dense decode; combine launch included in the timing)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src,
+                     "bytes_per_launch": dense_avg_bytes, "launch_ms": dense_launch,
+                     "traffic": TRAFFIC_PER_DENSE_LAUNCH},
+        "gpu_launches": r.launches_per_step * K,
+        "e2e": e2e,
+        "clocks": clock_info,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb, ct, desc = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cb / ct / 1e9, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                "sample": desc + " (%.1f s)" % ct}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one dense-decode launch of
+# attn_partial_kernel, scaled to this workload (None until measured).
+TRAFFIC_PER_DENSE_LAUNCH = None
+
+
+def run_e2e(w, r, steps, world):
+    """Same step, with every per-step input copied from pinned host memory and
+    every result copied back inside the timed region."""
+    ins = [w.q_verify] + w.q_dense + w.q_draft + [w.spec.p_logits, w.spec.q_logits, w.spec.draft_tokens]
+    outs = w.out_dense + [w.out_verify, w.mass, w.sel, w.cnt] + w.out_draft + [w.out_tokens, w.n_acc]
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def one():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        r.step()
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = allreduce_max(a.elapsed_time(b), world) / steps
+    return {"value": world * w.step_bytes / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("s3r", "reference"), default="s3r")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="fewer sequences than the 256 of the workload (small profiling case only)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "s3r":
+        print("note: fewer than 3 warm-up steps; timing rules want >= 3", file=sys.stderr)
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_s3r(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())
