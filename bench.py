@@ -318,7 +318,8 @@ def oracle_sample(seconds, seed=0):
     done_bytes = 0.0
     t0 = time.perf_counter()
     seqs_done = 0
-    for s in range(n_seqs):
+    for it in range(1 << 20):
+        s = it % n_seqs
         one = [s]
         for j in range(k):
             oracle.dense_decode_attn(qd, kp, vp, bt, L + j + 1, 1.0, seqs=one)
@@ -340,10 +341,10 @@ def oracle_sample(seconds, seed=0):
         oracle.spec_sample(p_l[one], q_l[one], x_l[one], sc.philox_seed, 0, seq_ids=one)
         done_bytes += (2 * sc.k + 1) * sc.vocab * 4
         seqs_done += 1
-        if time.perf_counter() - t0 >= seconds:
+        if time.perf_counter() - t0 >= seconds or (seconds <= 0 and seqs_done == n_seqs):
             break
     dt = time.perf_counter() - t0
-    desc = (f"{seqs_done} whole sequence(s) of the 256-sequence step (same recipe, histories U{{4096..16384}}): "
+    desc = (f"{seqs_done} sequence passes over {min(seqs_done, n_seqs)} distinct sequences of the 256-sequence step (same recipe, histories U{{4096..16384}}): "
             f"{k} dense decode steps, verify+mass, select, {k} sparse drafts, spec sample over V={sc.vocab}; "
             f"fp64 NumPy oracle")
     return done_bytes, dt, desc
@@ -501,7 +502,7 @@ def run_s3r(args, world, rank, local):
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
                      "bytes_per_launch": dense_avg_bytes, "launch_ms": dense_launch,
-                     "traffic": TRAFFIC_PER_DENSE_LAUNCH},
+                     "traffic": (DENSE_TRAFFIC_RATIO * dense_avg_bytes) if DENSE_TRAFFIC_RATIO else None},
         "gpu_launches": r.launches_per_step * K,
         "e2e": e2e,
         "clocks": clock_info,
@@ -515,9 +516,12 @@ def run_s3r(args, world, rank, local):
     return 0
 
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one dense-decode launch of
-# attn_partial_kernel, scaled to this workload (None until measured).
-TRAFFIC_PER_DENSE_LAUNCH = None
+# (dram__bytes_read.sum + dram__bytes_write.sum) / algorithmic bytes of one
+# dense-decode launch of attn_partial_kernel, from an ncu capture of the
+# 32-sequence case of this workload; traffic grows with the KV streamed, so the
+# full launch's traffic is this ratio times its algorithmic bytes.  None when
+# the kernel has changed since the capture.
+DENSE_TRAFFIC_RATIO = (1347936768 + 3411200) / 1346994176
 
 
 def run_e2e(w, r, steps, world):
@@ -556,7 +560,7 @@ def run_e2e(w, r, steps, world):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("s3r", "reference"), default="s3r")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
