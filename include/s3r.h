@@ -231,6 +231,37 @@ S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
                            uint64_t seed, uint64_t offset, int32_t* out_tokens,
                            int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
 
+/* Bytes of library-owned device scratch behind s3r_spec_sample_noalloc, held
+ * once by every GPU that loads the library until the process exits. */
+#define S3R_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
+
+/*
+ * s3r_spec_sample for callers that cannot allocate device memory: code whose
+ * device memory is one pool reserved up front, plugins that are handed only
+ * their input and output buffers, runtimes that forbid cudaMalloc once they
+ * are serving.  The S³R pages have no counterpart to this call; it exists
+ * only for such callers.
+ *
+ * Same arguments, semantics and results as s3r_spec_sample, without ws and
+ * ws_bytes.  Its scratch is a fixed S3R_NOALLOC_SCRATCH_BYTES array in the
+ * library's device image, so it never calls cudaMalloc, cudaFree or any
+ * allocating routine.
+ *   device_error  optional (NULL to skip) device int32 that receives this
+ *                 call's device error bits (the S3R_DEVERR_* values)
+ * Returns S3R_ERR_UNSUPPORTED, before enqueuing anything, when
+ * s3r_spec_sample_workspace_size(n, k) exceeds S3R_NOALLOC_SCRATCH_BYTES
+ * (for example n = 2048 with k = 8 needs 278,784 bytes and fits).
+ * The first call on each device looks up the array's device address (a
+ * one-time set-up per device, with that device current): make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * array and overwrites it, so calls whose work may overlap on the GPU
+ * (different streams without ordering) race and must not be issued.
+ */
+S3R_API s3r_status s3r_spec_sample_noalloc(const float* p_logits, const float* q_logits,
+                                   const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
+                                   uint64_t seed, uint64_t offset, int32_t* out_tokens,
+                                   int32_t* n_accepted, int32_t* device_error, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

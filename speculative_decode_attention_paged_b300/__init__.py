@@ -29,6 +29,7 @@ __all__ = [
     "s3r_verify_attn",
     "s3r_select_draft_pages",
     "s3r_spec_sample",
+    "s3r_spec_sample_noalloc",
     "DEVERR_BAD_PAGE",
     "DEVERR_BAD_LENGTH",
     "DEVERR_BAD_TOKEN",
@@ -97,6 +98,8 @@ _SIG = {
                                               _I32, _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64, _P, _P,
                                        _P, ctypes.c_size_t, _P]),
+    "s3r_spec_sample_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
+                                               _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -289,4 +292,27 @@ def s3r_spec_sample(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, 
     _call("s3r_spec_sample", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1), _I32(V),
           ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), ws.ptr(),
           ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return out_tokens, n_accepted
+
+
+NOALLOC_SCRATCH_BYTES = 2 * 1024 * 1024
+
+
+def s3r_spec_sample_noalloc(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, n_accepted,
+                            device_error=None, stream=None):
+    """s3r_spec_sample without a workspace, for callers that cannot allocate
+    device memory; the scratch lives in the library (see include/s3r.h).
+    device_error: optional int32 CUDA tensor of one element that receives the
+    call's device error bits."""
+    _need(p_logits, torch.float32, "p_logits")
+    _need(q_logits, torch.float32, "q_logits")
+    _need(draft_tokens, torch.int32, "draft_tokens")
+    _need(out_tokens, torch.int32, "out_tokens")
+    _need(n_accepted, torch.int32, "n_accepted")
+    if device_error is not None:
+        _need(device_error, torch.int32, "device_error")
+    n, k1, V = p_logits.shape
+    _call("s3r_spec_sample_noalloc", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1),
+          _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted),
+          _ptr(device_error), _stream(stream))
     return out_tokens, n_accepted
