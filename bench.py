@@ -166,7 +166,8 @@ class Runner:
         dev = w.kv.k_pool.device
         self.ws = s3r.Workspace(s3r.s3r_attn_workspace_size(self.desc, w.k), device=dev)
         self.sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(w.N, w.scfg.k), device=dev)
-        self.launches_per_step = 2 * w.k + 2 + 1 + 2 * w.k + 2
+        # dense (partial + combine) x k, verify x 2, select, drafts x 2k, sampler x 4
+        self.launches_per_step = 2 * w.k + 2 + 1 + 2 * w.k + 4
 
     def step(self, ev=None):
         """ev: list of 2k+4 events recorded at the phase boundaries, or None."""

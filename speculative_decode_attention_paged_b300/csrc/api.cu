@@ -9,16 +9,13 @@
 
 #include "attn_paged.cuh"
 #include "s3r_device.cuh"
+#include "spec_sample.cuh"
 
 namespace s3r {
 cudaError_t launch_select_pages(const float* mass, const int32_t* sel_lens, int S, int Hkv,
                                 int stride, double budget, int n_sink, int n_recent,
                                 int32_t* sel_pages, int32_t* sel_count, int b_max, int* err,
                                 cudaStream_t stream);
-cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
-                               int V, uint64_t seed, uint32_t offset, float2* stats,
-                               int32_t* out_tokens, int32_t* n_accepted, int* err,
-                               cudaStream_t stream);
 }  // namespace s3r
 
 namespace {
@@ -203,7 +200,7 @@ s3r_status s3r_attn_workspace_size(const s3r_paged_kv* kv, int32_t max_block_row
 s3r_status s3r_spec_sample_workspace_size(int32_t n, int32_t k, size_t* bytes) {
   if (bytes == nullptr || n < 0 || k < 0) return S3R_ERR_INVALID_ARG;
   if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
-  *bytes = 256 + ((static_cast<size_t>(n) * (2 * k + 1) * sizeof(float2) + 255) & ~size_t(255));
+  *bytes = spec_workspace_layout(n, k).total;
   return S3R_OK;
 }
 
@@ -290,16 +287,15 @@ s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
   if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
   if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
   if (static_cast<int64_t>(n) * (k + 1) * vocab > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(n) * std::max(2 * k + 1, kSampleChunks) > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
   size_t need = 0;
   s3r_spec_sample_workspace_size(n, k, &need);
   if (ws == nullptr || !aligned256(ws) || ws_bytes < need) return S3R_ERR_WORKSPACE;
   if (n == 0) return S3R_OK;
   if (p_logits == nullptr || out_tokens == nullptr || n_accepted == nullptr) return S3R_ERR_INVALID_ARG;
   if (k > 0 && (q_logits == nullptr || draft_tokens == nullptr)) return S3R_ERR_INVALID_ARG;
-  uint8_t* w = static_cast<uint8_t*>(ws);
   return to_status(launch_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
-                                      static_cast<uint32_t>(offset), reinterpret_cast<float2*>(w + 256),
-                                      out_tokens, n_accepted, reinterpret_cast<int*>(w),
+                                      static_cast<uint32_t>(offset), ws, out_tokens, n_accepted,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -7,29 +7,32 @@
 // from the residual distribution (rit.work, "Как разреженный черновик
 // сохраняет ответы плотной модели"; rebasdaily.com, "草稿可以稀疏，交卷必须完整").
 //
-// Two kernels:
-//   row_stats     one CTA per logit row (k+1 target rows and k draft rows per
-//                 sequence): the row max m and z = sum_v 2^((x_v - m) log2 e),
-//                 one streaming pass with 16-byte loads;
-//   decide        one CTA per sequence: the k ratio tests p_i(x_i)/q_i(x_i)
-//                 against Philox uniforms (fp64 ratio from fp32 row stats),
-//                 then an inverse CDF in token-id order over the residual
-//                 max(0, p - q) (or p_{k+1} for the bonus): each warp owns a
-//                 contiguous segment of the row; warp-scan step sums are
-//                 accumulated in fp64; the warp whose segment holds u * Z
-//                 rescans it with the same arithmetic to find the token.
+// Four kernels, all parallel over rows or chunks of rows:
+//   row_stats   one CTA per logit row (k+1 target rows and k draft rows per
+//               sequence): the row max m and z = sum_v 2^((x_v - m) log2 e),
+//               one streaming pass with 16-byte loads;
+//   accept      one warp per sequence: the k ratio tests p_i(x_i)/q_i(x_i)
+//               against Philox uniforms (fp64 ratio from fp32 row stats);
+//               a = the first rejected position (k if none);
+//   chunk_sum   one CTA per (sequence, chunk of the row): fp64 sums over the
+//               chunk of the residual max(0, p_a - q_a) (or of p_k for the
+//               bonus token) and of p_a (the fallback when the residual
+//               vanishes);
+//   pick        one CTA per sequence: the chunk sums locate the chunk holding
+//               u * Z; that chunk alone is scanned in token-id order (fp64
+//               prefix over contiguous per-thread runs) to find the token.
 
 #include <cfloat>
 
 #include "philox.cuh"
 #include "s3r_device.cuh"
+#include "spec_sample.cuh"
 
 namespace s3r {
 
 namespace {
 
 constexpr int kStatThreads = 256;
-constexpr int kDecideWarps = 8;
 constexpr double kLog2eD = 1.4426950408889634074;
 
 // 2^((x - m) log2 e) with m pre-scaled: mlog2 = m * log2 e.
@@ -121,196 +124,290 @@ __global__ void __launch_bounds__(kStatThreads)
   }
 }
 
-struct ResidualRow {
+// The row a sequence samples from, in probability space: the residual
+// max(0, p(v) - q(v)) after a rejection, or p(v) itself for the bonus token
+// (q == null).  One inline function, so every kernel computes the same values.
+struct SampleRow {
   const float* p;
-  const float* q;   // null -> sample from p itself
-  float mp, izp, mq, izq;
-  int V;
-  __device__ __forceinline__ float at(int v) const {
-    const float pv = scaled_exp(__ldg(p + v), mp) * izp;
+  const float* q;
+  float mp, izp, mq, izq;   // row max * log2 e and 1 / sum, target and draft
+  __device__ __forceinline__ float value(float lp, float lq) const {
+    const float pv = scaled_exp(lp, mp) * izp;
     if (q == nullptr) return pv;
-    return fmaxf(pv - scaled_exp(__ldg(q + v), mq) * izq, 0.f);
+    return fmaxf(pv - scaled_exp(lq, mq) * izq, 0.f);
   }
-  // The four values a lane owns in one 128-element step (0 beyond V).
-  __device__ __forceinline__ void four(int e0, float (&r)[4]) const {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = e0 + i < V ? at(e0 + i) : 0.f;
+  __device__ __forceinline__ float at(int v) const {
+    return value(__ldg(p + v), q != nullptr ? __ldg(q + v) : 0.f);
   }
 };
 
-__global__ void __launch_bounds__(kDecideWarps * 32)
-    decide_kernel(const float* __restrict__ p, const float* __restrict__ q,
-                  const int32_t* __restrict__ drafts, int N, int k, int V, uint64_t seed,
-                  uint32_t offset, const float2* __restrict__ stats, int32_t* __restrict__ out_tokens,
-                  int32_t* __restrict__ n_accepted, int* err) {
-  __shared__ int s_acc[64];
-  __shared__ double s_wtot[kDecideWarps];
-  __shared__ int s_token;
-  const int n = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int np_rows = N * (k + 1);
-
-  if (tid < k) {
-    const int x = __ldg(drafts + static_cast<int64_t>(n) * k + tid);
-    bool acc = false;
-    if (x < 0 || x >= V) {
-      report_error(err, S3R_DEVERR_BAD_TOKEN);
-    } else {
-      const float lp = __ldg(p + (static_cast<int64_t>(n) * (k + 1) + tid) * V + x);
-      const float lq = __ldg(q + (static_cast<int64_t>(n) * k + tid) * V + x);
-      const float2 sp = stats[static_cast<int64_t>(n) * (k + 1) + tid];
-      const float2 sq = stats[np_rows + static_cast<int64_t>(n) * k + tid];
-      const double e = (static_cast<double>(lp) - sp.x) - (static_cast<double>(lq) - sq.x);
-      const double ratio = exp2(e * kLog2eD) * static_cast<double>(sq.y) / static_cast<double>(sp.y);
-      const float u = philox_uniform(seed, offset, n, tid, kStreamAccept);
-      acc = static_cast<double>(u) < ratio;
-    }
-    s_acc[tid] = acc ? 1 : 0;
-  }
-  if (tid == 0) s_token = -1;
-  __syncthreads();
-  int a = k;
-  for (int i = 0; i < k; ++i) {
-    if (!s_acc[i]) {
-      a = i;
-      break;
-    }
-  }
-
+__device__ __forceinline__ SampleRow sample_row(const float* p, const float* q, const float2* stats,
+                                                int N, int k, int V, int n, int a, bool use_p) {
+  SampleRow row;
   const float2 sp = stats[static_cast<int64_t>(n) * (k + 1) + a];
-  ResidualRow row;
   row.p = p + (static_cast<int64_t>(n) * (k + 1) + a) * V;
   row.mp = sp.x * kLog2e;
   row.izp = 1.f / sp.y;
-  row.V = V;
   row.q = nullptr;
   row.mq = 0.f;
   row.izq = 0.f;
-  if (a < k) {
-    const float2 sq = stats[np_rows + static_cast<int64_t>(n) * k + a];
+  if (a < k && !use_p) {
+    const float2 sq = stats[static_cast<int64_t>(N) * (k + 1) + static_cast<int64_t>(n) * k + a];
     row.q = q + (static_cast<int64_t>(n) * k + a) * V;
     row.mq = sq.x * kLog2e;
     row.izq = 1.f / sq.y;
   }
-  const float u = philox_uniform(seed, offset, n, a, kStreamResample);
+  return row;
+}
 
-  const int steps = (V + 127) / 128;
-  const int per_warp = (steps + kDecideWarps - 1) / kDecideWarps;
-  const int s_begin = min(warp * per_warp, steps), s_end = min(s_begin + per_warp, steps);
+// Contiguous chunk `c` of a row of V tokens: [lo, hi).  The chunk length is a
+// multiple of 4 so float4 loads stay aligned when V is.
+__device__ __forceinline__ int chunk_len(int V) {
+  return ((V + kSampleChunks - 1) / kSampleChunks + 3) & ~3;
+}
 
-  // Step sums of one warp's segment: lane-local sequential sums of 4 values,
-  // then a Hillis-Steele warp inclusive scan; the same code runs in both passes.
-  auto step_scan = [&](int st, float (&r)[4], float& local, float& incl) {
-    row.four(st * 128 + lane * 4, r);
-    local = ((r[0] + r[1]) + r[2]) + r[3];
-    incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-  };
-
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    double wt = 0.0;
-    for (int st = s_begin; st < s_end; ++st) {
-      float r[4], local, incl;
-      step_scan(st, r, local, incl);
-      wt += static_cast<double>(__shfl_sync(0xffffffffu, incl, 31));
-    }
-    if (lane == 0) s_wtot[warp] = wt;
-    __syncthreads();
-    double Z = 0.0;
-    for (int w = 0; w < kDecideWarps; ++w) Z += s_wtot[w];
-    if (!(Z > 0.0) && row.q != nullptr) {
-      // The residual vanished (p == q in floating point): sample from p.
-      row.q = nullptr;
-      __syncthreads();
-      continue;
-    }
-    const double target = static_cast<double>(u) * Z;
-    // The warp whose segment holds the target (else the last non-empty one).
-    int wsel = -1, wlast = -1;
-    double run = 0.0, wbase = 0.0, lastbase = 0.0;
-    for (int w = 0; w < kDecideWarps; ++w) {
-      if (s_wtot[w] > 0.0) {
-        wlast = w;
-        lastbase = run;
+// One warp per sequence: the k ratio tests.  Draft x_i is accepted iff
+// u(n, i-1, ACCEPT) < p_i(x_i) / q_i(x_i); the ratio is formed in fp64 from the
+// fp32 logits and row statistics.  Writes a = index of the first rejection
+// (k if none), the accepted drafts and the -1 padding after position a.
+__global__ void __launch_bounds__(256)
+    accept_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                  const int32_t* __restrict__ drafts, int N, int k, int V, uint64_t seed,
+                  uint32_t offset, const float2* __restrict__ stats, int32_t* __restrict__ accept,
+                  int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (n >= N) return;
+  const int np_rows = N * (k + 1);
+  int first = k;
+  for (int base = 0; base < k; base += 32) {
+    const int i = base + lane;
+    bool rej = false;
+    if (i < k) {
+      const int x = __ldg(drafts + static_cast<int64_t>(n) * k + i);
+      if (x < 0 || x >= V) {
+        report_error(err, S3R_DEVERR_BAD_TOKEN);
+        rej = true;
+      } else {
+        const float lp = __ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x);
+        const float lq = __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x);
+        const float2 sp = stats[static_cast<int64_t>(n) * (k + 1) + i];
+        const float2 sq = stats[np_rows + static_cast<int64_t>(n) * k + i];
+        const double e = (static_cast<double>(lp) - sp.x) - (static_cast<double>(lq) - sq.x);
+        const double ratio = exp2(e * kLog2eD) * static_cast<double>(sq.y) / static_cast<double>(sp.y);
+        const float u = philox_uniform(seed, offset, n, i, kStreamAccept);
+        rej = !(static_cast<double>(u) < ratio);
       }
-      if (wsel < 0 && run + s_wtot[w] > target) {
-        wsel = w;
-        wbase = run;
-      }
-      run += s_wtot[w];
     }
-    if (wsel < 0) {
-      wsel = wlast;
-      wbase = lastbase;
-    }
-    if (warp == wsel) {
-      double running = wbase;
-      int last_pos = -1;   // last token with r > 0 seen so far (fallback)
-      int found = -1;
-      for (int st = s_begin; st < s_end && found < 0; ++st) {
-        float r[4], local, incl;
-        step_scan(st, r, local, incl);
-        const float step_total = __shfl_sync(0xffffffffu, incl, 31);
-        int lp = -1;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (r[i] > 0.f) lp = st * 128 + lane * 4 + i;
-        const unsigned has = __ballot_sync(0xffffffffu, lp >= 0);
-        if (has) last_pos = __shfl_sync(0xffffffffu, lp, 31 - __clz(has));
-        if (running + static_cast<double>(step_total) > target) {
-          const unsigned cross = __ballot_sync(0xffffffffu, running + static_cast<double>(incl) > target);
-          const int ls = __ffs(cross) - 1;
-          const float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-          int pick = -1;
-          if (lane == ls) {
-            const double base = running + (lane > 0 ? static_cast<double>(excl) : 0.0);
-            float part = 0.f;
-            int lastpos = -1;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              part += r[i];
-              if (r[i] > 0.f) lastpos = st * 128 + lane * 4 + i;
-              if (pick < 0 && r[i] > 0.f && base + static_cast<double>(part) > target)
-                pick = st * 128 + lane * 4 + i;
-            }
-            if (pick < 0) pick = lastpos;
-          }
-          pick = __shfl_sync(0xffffffffu, pick, ls);
-          found = pick >= 0 ? pick : last_pos;
-        }
-        running += static_cast<double>(step_total);
-      }
-      if (found < 0) found = last_pos;
-      if (lane == 0) s_token = found >= 0 ? found : 0;
-    }
-    __syncthreads();
-    break;
+    const unsigned b = __ballot_sync(0xffffffffu, rej);
+    if (b != 0u && first == k) first = base + __ffs(b) - 1;
   }
-
   int32_t* out = out_tokens + static_cast<int64_t>(n) * (k + 1);
-  for (int i = tid; i <= k; i += blockDim.x) {
-    int32_t v = -1;
-    if (i < a) v = __ldg(drafts + static_cast<int64_t>(n) * k + i);
-    else if (i == a) v = s_token >= 0 ? s_token : 0;
-    out[i] = v;
+  for (int i = lane; i <= k; i += 32) {
+    if (i < first) out[i] = __ldg(drafts + static_cast<int64_t>(n) * k + i);
+    else if (i > first) out[i] = -1;
   }
-  if (tid == 0) n_accepted[n] = a;
+  if (lane == 0) {
+    accept[n] = first;
+    n_accepted[n] = first;
+  }
+}
+
+// Block-wide sum of two doubles (fixed reduction order); result in thread 0.
+template <int THREADS>
+__device__ __forceinline__ double2 block_sum2(double x, double y) {
+  __shared__ double2 s_w[THREADS / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+  }
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = make_double2(x, y);
+  __syncthreads();
+  double2 t = make_double2(0.0, 0.0);
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < THREADS / 32; ++w) {
+      t.x += s_w[w].x;
+      t.y += s_w[w].y;
+    }
+  }
+  return t;
+}
+
+// One CTA per (sequence, chunk): the sums over the chunk of the residual row
+// max(0, p_a - q_a) and of p_a itself (the fallback when the residual
+// vanishes), or of p_k twice for the bonus row.  Coalesced 16-byte loads.
+template <bool VEC>
+__global__ void __launch_bounds__(256)
+    chunk_sum_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
+                     const float2* __restrict__ stats, const int32_t* __restrict__ accept,
+                     double2* __restrict__ chunk_sums) {
+  const int n = blockIdx.x / kSampleChunks;
+  const int c = blockIdx.x - n * kSampleChunks;
+  const int tid = threadIdx.x;
+  const int a = __ldg(accept + n);
+  const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, false);
+  const SampleRow prow = sample_row(p, q, stats, N, k, V, n, a, true);
+  const int CL = chunk_len(V);
+  const int lo = min(c * CL, V), hi = min(lo + CL, V);
+  float sr = 0.f, sp = 0.f;
+  if (VEC) {
+    const float4* p4 = reinterpret_cast<const float4*>(row.p + lo);
+    const float4* q4 = row.q != nullptr ? reinterpret_cast<const float4*>(row.q + lo) : nullptr;
+    const int n4 = (hi - lo) >> 2;
+    for (int b = tid; b < n4; b += 4 * 256) {
+      float4 lp[4], lq[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = b + j * 256;
+        lp[j] = i < n4 ? p4[i] : make_float4(-__builtin_huge_valf(), -__builtin_huge_valf(),
+                                              -__builtin_huge_valf(), -__builtin_huge_valf());
+        lq[j] = (q4 != nullptr && i < n4) ? q4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        sr += ((row.value(lp[j].x, lq[j].x) + row.value(lp[j].y, lq[j].y)) +
+               (row.value(lp[j].z, lq[j].z) + row.value(lp[j].w, lq[j].w)));
+        sp += ((prow.value(lp[j].x, 0.f) + prow.value(lp[j].y, 0.f)) +
+               (prow.value(lp[j].z, 0.f) + prow.value(lp[j].w, 0.f)));
+      }
+    }
+  } else {
+    for (int v = lo + tid; v < hi; v += 256) {
+      const float lp = __ldg(row.p + v);
+      sr += row.value(lp, row.q != nullptr ? __ldg(row.q + v) : 0.f);
+      sp += prow.value(lp, 0.f);
+    }
+  }
+  const double2 t = block_sum2<256>(static_cast<double>(sr), static_cast<double>(sp));
+  if (tid == 0) chunk_sums[blockIdx.x] = t;
+}
+
+// One CTA per sequence: inverse CDF in token-id order.  The chunk sums give
+// the chunk holding u * Z; its tokens are split into contiguous runs, one per
+// thread, whose fp64 sums are prefix-summed in thread order; the thread whose
+// run spans the target walks it to the token.
+__global__ void __launch_bounds__(256)
+    pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
+                uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
+                const int32_t* __restrict__ accept, const double2* __restrict__ chunk_sums,
+                int32_t* __restrict__ out_tokens) {
+  __shared__ double s_excl[257];
+  __shared__ int s_chunk, s_use_p, s_pick, s_last;
+  __shared__ double s_tgt;
+  const int n = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int a = __ldg(accept + n);
+  if (tid == 0) {
+    const double2* cs = chunk_sums + static_cast<int64_t>(n) * kSampleChunks;
+    double zr = 0.0;
+    for (int c = 0; c < kSampleChunks; ++c) zr += cs[c].x;
+    const bool use_p = (a == k) || !(zr > 0.0);
+    double Z = 0.0;
+    for (int c = 0; c < kSampleChunks; ++c) Z += use_p ? cs[c].y : cs[c].x;
+    const double target = static_cast<double>(philox_uniform(seed, offset, n, a, kStreamResample)) * Z;
+    // First chunk whose inclusive prefix exceeds the target, else the last
+    // chunk with positive mass.
+    double run = 0.0, base = 0.0, last_base = 0.0;
+    int pick = -1, last = 0;
+    for (int c = 0; c < kSampleChunks; ++c) {
+      const double v = use_p ? cs[c].y : cs[c].x;
+      if (v > 0.0) {
+        last = c;
+        last_base = run;
+      }
+      if (pick < 0 && run + v > target) {
+        pick = c;
+        base = run;
+      }
+      run += v;
+    }
+    if (pick < 0) {
+      pick = last;
+      base = last_base;
+    }
+    s_chunk = pick;
+    s_use_p = use_p ? 1 : 0;
+    s_tgt = target - base;
+    s_pick = 0x7fffffff;
+    s_last = -1;
+  }
+  __syncthreads();
+  const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, s_use_p != 0);
+  const int CL = chunk_len(V);
+  const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
+  const int E = (hi - lo + 255) / 256;
+  const int r0 = min(lo + tid * E, hi), r1 = min(r0 + E, hi);
+  double part = 0.0;
+  int my_last = -1;
+  for (int v = r0; v < r1; ++v) {
+    const float r = row.at(v);
+    part += static_cast<double>(r);
+    if (r > 0.f) my_last = v;
+  }
+  s_excl[tid] = part;
+  if (my_last >= 0) atomicMax(&s_last, my_last);
+  __syncthreads();
+  if (tid == 0) {
+    // Exclusive prefix in thread order, sequential so it is monotone.
+    double run = 0.0;
+    for (int t = 0; t < 256; ++t) {
+      const double v = s_excl[t];
+      s_excl[t] = run;
+      run += v;
+    }
+    s_excl[256] = __longlong_as_double(0x7ff0000000000000LL);   // +inf
+  }
+  __syncthreads();
+  const double tgt = s_tgt;
+  if (s_excl[tid] <= tgt && tgt < s_excl[tid + 1]) {
+    double run = s_excl[tid];
+    int pick = -1;
+    for (int v = r0; v < r1; ++v) {
+      const float r = row.at(v);
+      run += static_cast<double>(r);
+      if (r > 0.f && run > tgt) {
+        pick = v;
+        break;
+      }
+    }
+    if (pick < 0) pick = my_last;
+    if (pick >= 0) atomicMin(&s_pick, pick);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int tok = s_pick != 0x7fffffff ? s_pick : s_last;
+    if (tok < 0) tok = lo < V ? lo : V - 1;
+    out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
+  }
 }
 
 }  // namespace
 
+SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
+  auto al = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  SpecWorkspaceLayout L{};
+  L.err_off = 0;
+  L.stats_off = 256;
+  L.accept_off = L.stats_off + al(static_cast<size_t>(N) * (2 * k + 1) * sizeof(float2));
+  L.chunk_off = L.accept_off + al(static_cast<size_t>(N) * sizeof(int32_t));
+  L.total = L.chunk_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(double2));
+  return L;
+}
+
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
-                               int V, uint64_t seed, uint32_t offset, float2* stats,
-                               int32_t* out_tokens, int32_t* n_accepted, int* err,
-                               cudaStream_t stream) {
+                               int V, uint64_t seed, uint32_t offset, void* ws,
+                               int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream) {
   if (N == 0) return cudaSuccess;
+  const SpecWorkspaceLayout L = spec_workspace_layout(N, k);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* err = reinterpret_cast<int*>(w + L.err_off);
+  float2* stats = reinterpret_cast<float2*>(w + L.stats_off);
+  int32_t* accept = reinterpret_cast<int32_t*>(w + L.accept_off);
+  double2* chunks = reinterpret_cast<double2*>(w + L.chunk_off);
   const int rows = N * (2 * k + 1);
   const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
-                   (reinterpret_cast<uintptr_t>(q) % 16 == 0);
+                   (k == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
   if (vec) {
     row_stats_kernel<true><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats);
   } else {
@@ -318,8 +415,21 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decide_kernel<<<N, kDecideWarps * 32, 0, stream>>>(p, q, drafts, N, k, V, seed, offset, stats,
-                                                      out_tokens, n_accepted, err);
+  accept_kernel<<<(N + 7) / 8, 256, 0, stream>>>(p, q, drafts, N, k, V, seed, offset, stats, accept,
+                                                  out_tokens, n_accepted, err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t chunk_blocks = static_cast<int64_t>(N) * kSampleChunks;
+  if (vec) {
+    chunk_sum_kernel<true><<<static_cast<unsigned>(chunk_blocks), 256, 0, stream>>>(p, q, N, k, V, stats,
+                                                                                   accept, chunks);
+  } else {
+    chunk_sum_kernel<false><<<static_cast<unsigned>(chunk_blocks), 256, 0, stream>>>(p, q, N, k, V, stats,
+                                                                                    accept, chunks);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  pick_kernel<<<N, 256, 0, stream>>>(p, q, N, k, V, seed, offset, stats, accept, chunks, out_tokens);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,30 @@
+// Exact speculative sampler: workspace layout and host launch interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace s3r {
+
+// Each residual (or bonus) row is cut into this many contiguous chunks; the
+// chunk sums locate the inverse-CDF target before one chunk is scanned.
+constexpr int kSampleChunks = 32;
+
+struct SpecWorkspaceLayout {
+  size_t err_off;     // device error word (first 256 bytes)
+  size_t stats_off;   // float2 [N][2k+1]: (row max, sum of exp(x - max))
+  size_t accept_off;  // int32 [N]: accepted count a = index of the row sampled from
+  size_t chunk_off;   // double2 [N][kSampleChunks]: (residual sum, target-row sum) per chunk
+  size_t total;
+};
+
+SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k);
+
+// Enqueue the four sampler kernels.  `ws` is the caller's workspace laid out
+// by spec_workspace_layout(N, k).
+cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
+                               int V, uint64_t seed, uint32_t offset, void* ws,
+                               int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream);
+
+}  // namespace s3r
