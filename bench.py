@@ -558,6 +558,244 @@ def run_e2e(w, r, steps, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+# ---------------------------------------------------------------- extra workloads (one JSON line each)
+
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _visible_draft_tokens(sel, cnt, sel_lens, j):
+    """Tokens all (sequence, KV head) pairs of draft step j read."""
+    sel = sel.cpu().numpy().astype(np.int64)
+    cnt = cnt.cpu().numpy()
+    L = sel_lens.cpu().numpy().astype(np.int64)
+    total = 0
+    S, H, _ = sel.shape
+    for s in range(S):
+        for h in range(H):
+            pg = sel[s, h, : cnt[s, h]]
+            total += int(np.minimum(pg * 16 + 16, L[s]).sum() - np.minimum(pg * 16, L[s]).sum())
+    return total + S * H * (j + 1)
+
+
+def _timed(fn, steps, warmup):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = _events(2)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def _clock_sampler():
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) is not None else None
+    c = ClockSampler(uuid)
+    c.start()
+    time.sleep(0.3)
+    return c
+
+
+def run_sweep(args):
+    """Qwen3-8B attention geometry, one layer: 128 sequences x U{8192..24576},
+    32 q / 8 KV heads, k = T = 8 (32 query rows per KV head in verify); a dense
+    decode step, verify with page mass, then per budget in {0.05, 0.10, 0.25,
+    0.50}: select + 8 sparse draft steps."""
+    import speculative_decode_attention_paged_b300 as s3r
+    dev = torch.device("cuda", torch.cuda.current_device())
+    c = ATTN_CONFIGS[3]
+    S = args.seqs or c.num_seqs
+    kv = make_paged_kv(S, c.q_heads, c.kv_heads, 2 * c.k, seed=c.seed, device=dev,
+                       hist_min=c.hist_min, hist_max=c.hist_max)
+    k, Hq, Hkv = c.k, c.q_heads, c.kv_heads
+    desc = s3r.PagedKVDesc(kv.k_pool, kv.v_pool, kv.block_table, Hq)
+    ws = s3r.Workspace(s3r.s3r_attn_workspace_size(desc, k), device=dev)
+    L = kv.hist_lens
+    qv = make_queries(kv, 3000, rows=k)
+    qd = [make_queries(kv, 3100 + j) for j in range(k)]
+    out_v = torch.empty(qv.shape, dtype=torch.float32, device=dev)
+    out_d = torch.empty(qd[0].shape, dtype=torch.float32, device=dev)
+    mass = torch.empty((S, Hkv, kv.max_pages), dtype=torch.float32, device=dev)
+    sel_lens = (L + k).to(torch.int32)
+    clocks = _clock_sampler()
+    Lsum = float(L.double().sum())
+    dense_bytes = (Lsum + S) * Hkv * KV_TOKEN_BYTES_PER_HEAD + S * Hq * 128 * 6
+    ctx = (L + 1).to(torch.int32)
+    t_dense = _timed(lambda: s3r.s3r_dense_decode_attn(desc, ctx, qd[0], out_d, 1.0, ws), args.steps, args.warmup)
+    verify_bytes = (Lsum + S * k) * Hkv * KV_TOKEN_BYTES_PER_HEAD + S * k * Hq * 128 * 6 + S * Hkv * kv.max_pages * 4
+    t_verify = _timed(lambda: s3r.s3r_verify_attn(desc, L, qv, out_v, 1.0, ws, page_mass=mass), args.steps,
+                      args.warmup)
+    budgets = {}
+    total_b, total_t = dense_bytes + verify_bytes, t_dense + t_verify
+    for budget in c.budgets:
+        b_max = selection_budget_pages(kv.max_pages, budget)
+        sel = torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev)
+        cnt = torch.empty((S, Hkv), dtype=torch.int32, device=dev)
+        t_sel = _timed(lambda: s3r.s3r_select_draft_pages(mass, sel_lens, budget, sel, cnt, ws), args.steps,
+                       args.warmup)
+        ws.check()
+        tok = [_visible_draft_tokens(sel, cnt, sel_lens, j) for j in range(k)]
+        dbytes = [t * KV_TOKEN_BYTES_PER_HEAD + S * Hq * 128 * 6 + S * Hkv * (b_max + 1) * 4 for t in tok]
+
+        def drafts():
+            for j in range(k):
+                s3r.s3r_sparse_draft_attn(desc, sel_lens, j, sel, cnt, qd[j], out_d, 1.0, ws)
+
+        t_d = _timed(drafts, max(1, args.steps // 2), args.warmup)
+        budgets[str(budget)] = {"draft_kv_gb_per_step": tok[0] * KV_TOKEN_BYTES_PER_HEAD / 1e9,
+                                "draft_ms_per_step": t_d / k, "draft_gbs": sum(dbytes) / (t_d * 1e-3) / 1e9,
+                                "select_ms": t_sel,
+                                "round_ms": t_d + t_verify + t_sel,
+                                "draft_verify_tokens_per_s": S * k / ((t_d + t_verify + t_sel) * 1e-3)}
+        total_b += sum(dbytes)
+        total_t += t_d
+    ws.check()
+    clock_info = clocks.stop()
+    return {"workload": f"qwen3-8b-geom 1 layer: {S} seqs x U{{8192..24576}}, 32 q / 8 kv heads, d=128, k=T=8",
+            "metric": METRIC, "value": total_b / (total_t * 1e-3) / 1e9, "unit": UNIT,
+            "dense": {"ms": t_dense, "gb": dense_bytes / 1e9, "gbs": dense_bytes / (t_dense * 1e-3) / 1e9},
+            "verify_T8_G4": {"ms": t_verify, "gb": verify_bytes / 1e9, "gbs": verify_bytes / (t_verify * 1e-3) / 1e9},
+            "budgets": budgets, "clocks": clock_info}
+
+
+def run_sampler(args):
+    """Exact speculative sampling at rollout scale: 2048 sequences (256 prompts
+    x 8 responses) x k = 8 over V = 151936, sigma in {0.3, 1.0}."""
+    import speculative_decode_attention_paged_b300 as s3r
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sc = SAMPLER_CONFIGS[4]
+    N = args.seqs or sc.num_seqs
+    res = {}
+    for sigma in sc.q_sigmas:
+        inp = make_spec_inputs(N, sc.k, sc.vocab, sc.p_sigma, sigma, sc.seed, device=dev)
+        ws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(N, sc.k), device=dev)
+        out = torch.empty((N, sc.k + 1), dtype=torch.int32, device=dev)
+        nacc = torch.empty((N,), dtype=torch.int32, device=dev)
+        clocks = _clock_sampler()
+        t = _timed(lambda: s3r.s3r_spec_sample(inp.p_logits, inp.q_logits, inp.draft_tokens, sc.philox_seed, 0,
+                                               out, nacc, ws), args.steps, args.warmup)
+        clock_info = clocks.stop()
+        ws.check()
+        a = nacc.cpu().numpy()
+        nbytes = N * (2 * sc.k + 1) * sc.vocab * 4 + N * (2 * sc.k + 2) * 4
+        reached = np.array([(a >= i).sum() for i in range(sc.k)])
+        accepted = np.array([(a > i).sum() for i in range(sc.k)])
+        res[str(sigma)] = {"ms": t, "gb": nbytes / 1e9, "gbs": nbytes / (t * 1e-3) / 1e9,
+                           "mean_accepted": float(a.mean()), "mean_emitted": float((a + 1).mean()),
+                           "per_position_acceptance": [float(x) for x in accepted / np.maximum(reached, 1)],
+                           "accepted_histogram": np.bincount(a, minlength=sc.k + 1).tolist(),
+                           "sampled_tokens_per_s": float((a + 1).sum() / (t * 1e-3)), "clocks": clock_info}
+        del inp
+        torch.cuda.empty_cache()
+    vals = [r["gbs"] for r in res.values()]
+    return {"workload": f"spec sample: {N} seqs x k={sc.k} x V={sc.vocab} fp32, p~N(0,3^2), q=p+N(0,s^2)",
+            "metric": METRIC, "value": float(np.mean(vals)), "unit": UNIT, "sigma": res}
+
+
+def run_layers(args):
+    """Multi-layer draft-verify round: all 28 layers of the Qwen3-1.7B
+    attention geometry, 32 sequences with histories U{4096..16384} in a pool
+    sized for 16K tokens per sequence (~60 GB), per-layer random queries,
+    budget 0.05, k = T = 4.  A round = 4 sparse draft steps over all layers,
+    verify with page mass and selection for every layer (feeding the next
+    round's drafts), captured in one CUDA graph; compared with 4 dense decode
+    steps over all layers (a second graph)."""
+    import speculative_decode_attention_paged_b300 as s3r
+    dev = torch.device("cuda", torch.cuda.current_device())
+    c = ATTN_CONFIGS[5]
+    S, k, Hq, Hkv, n_layers = (args.seqs or c.num_seqs), c.k, c.q_heads, c.kv_heads, c.layers
+    if args.layers:
+        n_layers = args.layers
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(c.seed)
+    L = torch.randint(c.hist_min, c.hist_max + 1, (S,), generator=gen).to(torch.int32)
+    if args.all_16k:
+        L = torch.full((S,), c.capacity_tokens - 2 * k, dtype=torch.int32)
+    layers = []
+    for li in range(n_layers):
+        kv = make_paged_kv(S, Hq, Hkv, 2 * k, seed=c.seed * 1000 + li, device=dev, hist_lens=L.to(dev),
+                           capacity_tokens=c.capacity_tokens)
+        desc = s3r.PagedKVDesc(kv.k_pool, kv.v_pool, kv.block_table, Hq)
+        b_max = selection_budget_pages(kv.max_pages, c.budgets[0])
+        layers.append(dict(
+            kv=kv, desc=desc,
+            qv=make_queries(kv, 5000 + li, rows=k), qd=[make_queries(kv, 5100 + 16 * li + j) for j in range(k)],
+            out_v=torch.empty((S, k, Hq, 128), dtype=torch.float32, device=dev),
+            out_d=[torch.empty((S, Hq, 128), dtype=torch.float32, device=dev) for _ in range(k)],
+            mass=torch.empty((S, Hkv, kv.max_pages), dtype=torch.float32, device=dev),
+            sel=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
+            cnt=torch.empty((S, Hkv), dtype=torch.int32, device=dev)))
+    Ld = L.to(dev)
+    sel_lens = (Ld + k).to(torch.int32)
+    ctx = [(Ld + j + 1).to(torch.int32) for j in range(k)]
+    ws = s3r.Workspace(s3r.s3r_attn_workspace_size(layers[0]["desc"], k), device=dev)
+    pool_gb = sum(2 * l["kv"].k_pool.numel() * 2 for l in layers) / 1e9
+
+    def verify_select():
+        for l in layers:
+            s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
+            s3r.s3r_select_draft_pages(l["mass"], sel_lens, c.budgets[0], l["sel"], l["cnt"], ws)
+
+    def s3r_round():
+        for j in range(k):
+            for l in layers:
+                s3r.s3r_sparse_draft_attn(l["desc"], sel_lens, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0,
+                                          ws)
+        verify_select()
+
+    def dense_steps():
+        for j in range(k):
+            for l in layers:
+                s3r.s3r_dense_decode_attn(l["desc"], ctx[j], l["qd"][j], l["out_d"][j], 1.0, ws)
+
+    verify_select()           # selections for the first round's drafts
+    s3r_round()
+    dense_steps()
+    torch.cuda.synchronize()
+    ws.check()
+    # CUDA graphs: one per round, one per 4 dense steps (the calls enqueue on torch's current stream)
+    g_round, g_dense = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_round, stream=side, capture_error_mode="thread_local"):
+            s3r_round()
+        with torch.cuda.graph(g_dense, stream=side, capture_error_mode="thread_local"):
+            dense_steps()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    clocks = _clock_sampler()
+    t_round = _timed(g_round.replay, args.steps, args.warmup)
+    t_dense = _timed(g_dense.replay, args.steps, args.warmup)
+    t_round_eager = _timed(s3r_round, max(2, args.steps // 4), 1)
+    clock_info = clocks.stop()
+    ws.check()
+    Lsum = float(L.double().sum())
+    tok = [sum(_visible_draft_tokens(l["sel"], l["cnt"], sel_lens, j) for l in layers) for j in range(k)]
+    draft_bytes = sum(t * KV_TOKEN_BYTES_PER_HEAD for t in tok) + k * n_layers * S * Hq * 128 * 6
+    verify_bytes = n_layers * ((Lsum + S * k) * Hkv * KV_TOKEN_BYTES_PER_HEAD + S * k * Hq * 128 * 6
+                               + 2 * S * Hkv * layers[0]["kv"].max_pages * 4)
+    dense_bytes = n_layers * sum((Lsum + S * (j + 1)) * Hkv * KV_TOKEN_BYTES_PER_HEAD + S * Hq * 128 * 6
+                                 for j in range(k))
+    round_bytes = draft_bytes + verify_bytes
+    return {"workload": f"qwen3-1.7b-geom {n_layers} layers: {S} seqs x "
+                        + ("all 16K" if args.all_16k else "U{4096..16384}") + f" in a {pool_gb:.1f} GB pool, "
+                        f"budget 0.05, k=T=4, one CUDA graph per round",
+            "metric": METRIC, "value": round_bytes / (t_round * 1e-3) / 1e9, "unit": UNIT,
+            "round_ms": t_round, "round_ms_eager": t_round_eager, "round_gb": round_bytes / 1e9,
+            "dense_4_steps_ms": t_dense, "dense_gb": dense_bytes / 1e9,
+            "dense_gbs": dense_bytes / (t_dense * 1e-3) / 1e9,
+            "speedup_vs_dense": t_dense / t_round,
+            "draft_verify_tokens_per_s": S * k / (t_round * 1e-3),
+            "dense_tokens_per_s": S * k / (t_dense * 1e-3),
+            "launches_per_round": n_layers * (2 * k + 3), "clocks": clock_info}
+
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -566,6 +804,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("s3r", "reference"), default="s3r")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=("round", "sweep", "sampler", "layers"), default="round",
+                    help="round (default): the 256-sequence S3R round + dense baseline; sweep: Qwen3-8B "
+                         "geometry budget sweep; sampler: 2048 x k=8 sampler; layers: the 28-layer round")
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers for --workload layers")
+    ap.add_argument("--all-16k", action="store_true", help="--workload layers with every history at 16K")
     ap.add_argument("--seqs", type=int, default=None,
                     help="fewer sequences than the 256 of the workload (small profiling case only)")
     args = ap.parse_args(argv)
@@ -575,6 +818,16 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.workload != "round":
+            import speculative_decode_attention_paged_b300 as s3r
+            s3r.load_library()
+            leg = {"sweep": run_sweep, "sampler": run_sampler, "layers": run_layers}[args.workload]
+            line = leg(args)
+            line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+                         "data": "synthetic", "l2": "inputs larger than L2"})
+            if rank == 0:
+                print(json.dumps(line), flush=True)
+            return 0
         return run_s3r(args, world, rank, local)
     finally:
         if world > 1:
