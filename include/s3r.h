@@ -30,9 +30,11 @@
  *    call that set an error bit are unspecified but finite.
  *  - Workspace: one caller-allocated device buffer of at least the size that
  *    the *_workspace_size() queries return, 256-byte aligned.  Its first 256
- *    bytes hold the sticky error word; zero them once with
- *    s3r_workspace_init() after allocation.  Calls that share a workspace
- *    must be ordered (same stream or event-ordered).
+ *    bytes hold the sticky error word; the attention calls also keep
+ *    per-(sequence, KV head) arrival counters in it, which every call leaves
+ *    at zero.  Zero the whole buffer once with s3r_workspace_init() after
+ *    allocation, and again after a call reported S3R_DEVERR_TIMEOUT.  Calls
+ *    that share a workspace must be ordered (same stream or event-ordered).
  *  - KV cache layout: bf16 pools [num_phys_pages][num_kv_heads][16][128]
  *    (one page holds 16 tokens; head_dim 128), addressed through a block
  *    table [num_seqs][max_pages_per_seq] of int32 physical page ids.  Query
@@ -111,7 +113,7 @@ S3R_API s3r_status s3r_spec_sample_workspace_size(int32_t n, int32_t k, size_t* 
 /* Workspace bytes for s3r_select_draft_pages (host): the error word only. */
 S3R_API s3r_status s3r_select_workspace_size(size_t* bytes);
 
-/* Zero the workspace's error word (enqueued on `stream`). */
+/* Zero the whole workspace: error word and counters (enqueued on `stream`). */
 S3R_API s3r_status s3r_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /*
@@ -198,7 +200,8 @@ S3R_API s3r_status s3r_verify_attn(const s3r_paged_kv* kv, const int32_t* hist_l
  *   sel_pages int32 [num_seqs][num_kv_heads][b_max] out: ascending page ids,
  *             unused slots set to -1
  *   sel_count int32 [num_seqs][num_kv_heads] out: B
- * b_max must be at least the B of a history of mass_stride pages.
+ * b_max must be at least the B of a history of mass_stride pages;
+ * mass_stride above 49152 pages returns S3R_ERR_UNSUPPORTED.
  */
 S3R_API s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t* sel_lens, int32_t num_seqs,
                                   int32_t num_kv_heads, int32_t mass_stride, double budget,

@@ -24,6 +24,8 @@ using namespace s3r;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSpecK = 64;
+// Longest mass row the selection kernel stages in shared memory (pages).
+constexpr int kMaxSelectPages = 49152;
 
 int g_sm_count[kMaxDevices];
 std::once_flag g_encode_once;
@@ -84,6 +86,9 @@ s3r_status validate_kv(const s3r_paged_kv* kv) {
   if (kv->num_phys_pages > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(kv->max_pages_per_seq) * kPage > 0x3fffffff) return S3R_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(kv->num_seqs) * kv->num_kv_heads > kMaxPairs) return S3R_ERR_UNSUPPORTED;
+  // the global page stream is indexed with 32-bit counts
+  if (static_cast<int64_t>(kv->num_seqs) * kv->num_kv_heads * kv->max_pages_per_seq > 0x7fffffffLL)
+    return S3R_ERR_UNSUPPORTED;
   if (kv->num_seqs > 0) {
     if (kv->k_pool == nullptr || kv->v_pool == nullptr || kv->block_table == nullptr)
       return S3R_ERR_INVALID_ARG;
@@ -153,10 +158,9 @@ s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, 
   a.page_mass = page_mass;
   a.mass_stride = mass_stride;
   a.err = reinterpret_cast<int*>(w + lay.err_off);
-  a.chunk_prefix = reinterpret_cast<int*>(w + lay.prefix_off);
+  a.arrivals = reinterpret_cast<int*>(w + lay.arrivals_off);
   a.part_o = reinterpret_cast<float*>(w + lay.part_o_off);
   a.part_ml = reinterpret_cast<float*>(w + lay.part_ml_off);
-  a.row_lse = mass ? reinterpret_cast<float*>(w + lay.row_lse_off) : nullptr;
   a.page_lse = mass ? reinterpret_cast<float*>(w + lay.page_lse_off) : nullptr;
   a.total_warps = total_warps;
   a.n_pairs = n_pairs;
@@ -212,7 +216,7 @@ s3r_status s3r_select_workspace_size(size_t* bytes) {
 
 s3r_status s3r_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return S3R_ERR_WORKSPACE;
-  return to_status(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));
+  return to_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
 }
 
 s3r_status s3r_read_device_error(const void* ws, void* stream, int32_t* code, int32_t clear) {
@@ -262,6 +266,7 @@ s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t* sel_len
       b_max < 0)
     return S3R_ERR_INVALID_ARG;
   if (!(budget >= 0.0 && budget <= 1.0)) return S3R_ERR_INVALID_ARG;
+  if (mass_stride > kMaxSelectPages) return S3R_ERR_UNSUPPORTED;
   if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return S3R_ERR_WORKSPACE;
   if (static_cast<int64_t>(num_seqs) * num_kv_heads > 0x7fffffff) return S3R_ERR_UNSUPPORTED;
   if (num_seqs == 0) return S3R_OK;

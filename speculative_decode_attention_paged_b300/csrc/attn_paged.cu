@@ -15,9 +15,11 @@
 //     tile + a 4 KiB V tile, contiguous in the pool.  All pages of all pairs
 //     form one global stream; each warp of a persistent grid (one 8-warp CTA
 //     per SM) takes an equal contiguous share of it, so load balance is exact
-//     whatever the mix of context lengths.  A pair cut by a share boundary
-//     leaves a partial (m, l, O) per side; a small combine kernel merges them
-//     (log-sum-exp merge).  At most two partials per warp are written.
+//     whatever the mix of context lengths.  A pair cut by share boundaries
+//     leaves a partial (m, l, O) per segment (at most two per warp); each
+//     writer publishes its segment with a fence and an arrival counter, and
+//     the last segment to arrive merges them (log-sum-exp merge) in place, so
+//     one launch does the whole call.
 //   * Each warp runs its own 3-stage TMA pipeline (cp.async.bulk.tensor, one
 //     mbarrier per stage, 128-byte swizzle so ldmatrix reads are
 //     bank-conflict free).  Page ids are fetched 32 at a time, one per lane.
@@ -26,8 +28,8 @@
 //     16 tokens of a page as one n16 / k16 block, fp32 accumulation and an
 //     online softmax in registers (exp2 domain).
 //   * Verify with page mass also stores, per (page, row), the base-2
-//     log-sum-exp of the row's scores over the page; the combine turns it
-//     into the normalised mass sum_r 2^(lse_page,r - LSE_r).
+//     log-sum-exp of the row's scores over the page; the warp that completes
+//     a pair turns it into the normalised mass sum_r 2^(lse_page,r - LSE_r).
 //   * Data-dependent errors (bad page id, bad length) skip the page and set a
 //     bit in the device error word; every wait is bounded.
 
@@ -193,6 +195,21 @@ __device__ void block_exclusive_scan(int* vals, int n, int* scratch) {
   __syncthreads();
 }
 
+// Zero output rows (and zero page mass) of a pair with no page to read.
+__device__ void zero_pair(const AttnArgs& a, int pair) {
+  const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
+  for (int r = 0; r < a.R; ++r) {
+    const int i = r / a.G, g = r - (r / a.G) * a.G;
+    float4* dst = reinterpret_cast<float4*>(
+        a.out + ((static_cast<int64_t>(s) * a.T + i) * a.Hq + h * a.G + g) * kHeadDim);
+    for (int c = 0; c < kHeadDim / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (a.page_mass != nullptr) {
+    float* m = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
+    for (int lp = 0; lp < a.mass_stride; ++lp) m[lp] = 0.f;
+  }
+}
+
 // Smem address of the 16-byte chunk holding (token, d0..d0+7) of a swizzled
 // K or V tile: two 64-column halves of 16 rows x 128 B, 128B-swizzled.
 __device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int token, int d0) {
@@ -212,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kAttnWarps * kAttnStages * kStageBytes);
   int4* meta = reinterpret_cast<int4*>(bars + kAttnWarps * kAttnStages);   // 2 int4 per stage
   int* scratch = reinterpret_cast<int*>(meta + 2 * kAttnWarps * kAttnStages);   // 32 ints
-  int* prefix = scratch + 32;                                            // n_chunks + 1
+  float* lse_all = reinterpret_cast<float*>(scratch + 32);               // [warps][32] row LSEs
+  int* prefix = reinterpret_cast<int*>(lse_all + kAttnWarps * 32);       // n_chunks + 1
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -224,16 +242,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int c = warp; c < a.n_chunks; c += kAttnWarps) {
     const int pair = c * kPairChunk + lane;
     int np = 0;
-    if (pair < a.n_pairs) np = pair_geom(a, pair, blockIdx.x == 0).np;
+    if (pair < a.n_pairs) {
+      np = pair_geom(a, pair, blockIdx.x == 0).np;
+      // A pair with nothing to read gets zero rows (and zero mass) here.
+      if (np == 0 && (c % static_cast<int>(gridDim.x)) == static_cast<int>(blockIdx.x)) zero_pair(a, pair);
+    }
     np = warp_sum(np);
     if (lane == 0) prefix[c] = np;
   }
   fence_barrier_init();
   __syncthreads();
   block_exclusive_scan(prefix, a.n_chunks, scratch);
-  if (blockIdx.x == 0) {
-    for (int i = tid; i <= a.n_chunks; i += kThreads) a.chunk_prefix[i] = prefix[i];
-  }
 
   const int64_t N = prefix[a.n_chunks];
   const int tw = a.total_warps;
@@ -334,6 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float m_r[MT][2], l_r[MT][2];
   int cur_pair = -1, cur_s = 0, cur_h = 0, cur_L = 0, cur_np = 0, seg_first = 0, seg_last = 0;
   int seg_index = 0;
+  int64_t cur_start = 0;           // global stream index of the current pair's first page
+  float* my_lse = lse_all + warp * 32;
 
   // Per-lane constant parts of the ldmatrix row addresses.
   const int k_tok = ((lane >> 4) << 3) + (lane & 7);
@@ -375,6 +396,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
+  // Page mass of the current pair from the per-(page, row) log-sum-exps and
+  // the rows' final LSEs in my_lse; zero beyond its np pages.
+  auto write_mass = [&]() {
+    __syncwarp();
+    float* dst = a.page_mass + static_cast<int64_t>(cur_pair) * a.mass_stride;
+    const float* pl = a.page_lse + static_cast<int64_t>(cur_pair) * a.max_pages * a.R;
+    for (int lp = lane; lp < a.mass_stride; lp += 32) {
+      float mass = 0.f;
+      if (lp < cur_np) {
+        const float* e = pl + static_cast<int64_t>(lp) * a.R;
+        for (int r = 0; r < a.R; ++r) {
+          const float v = __ldcg(e + r);
+          const float L = my_lse[r];
+          if (v != kNegInf && L != kNegInf) mass += fast_exp2(v - L);
+        }
+      }
+      dst[lp] = mass;
+    }
+  };
+
+  // Slot of segment j of a pair cut by warp shares: the pair's pages start at
+  // global index X and span shares gwa..; with N >= tw every share holds a
+  // page, otherwise every non-empty share holds exactly one page.
+  auto segment_slot = [&](int64_t X, int gwa, int j) -> int {
+    if (N >= tw) return (gwa + j) * 2 + ((j == 0 && share_start(N, gwa, tw) < X) ? 1 : 0);
+    return share_of(N, X + j, tw) * 2;
+  };
+
+  // Merge the partials of the current (cut) pair: lane r < R folds row r's
+  // (m, l) over the segments, then every lane merges 4 of the 128 columns.
+  auto merge_pair = [&](int nseg, int gwa) {
+    float M = kNegInf, Ls = 0.f;
+    if (lane < a.R) {
+      for (int j = 0; j < nseg; ++j) {
+        const int slot = segment_slot(cur_start, gwa, j);
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+            a.part_ml + (static_cast<int64_t>(slot) * a.R + lane) * 2));
+        if (ml.y > 0.f) {
+          const float mn = fmaxf(M, ml.x);
+          Ls = Ls * fast_exp2(M - mn) + ml.y * fast_exp2(ml.x - mn);
+          M = mn;
+        }
+      }
+      if (MASS) my_lse[lane] = Ls > 0.f ? M + fast_log2(Ls) : kNegInf;
+    }
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    for (int r = 0; r < a.R; ++r) {
+      const float Mr = __shfl_sync(0xffffffffu, M, r);
+      const float ir = __shfl_sync(0xffffffffu, inv, r);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < nseg; ++j) {
+        const int slot = segment_slot(cur_start, gwa, j);
+        const int64_t row = static_cast<int64_t>(slot) * a.R + r;
+        const float mr = __ldcg(a.part_ml + row * 2);
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * kHeadDim) + lane);
+        const float w = mr == kNegInf ? 0.f : fast_exp2(mr - Mr) * ir;
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+      reinterpret_cast<float4*>(a.out + q_row_offset(r))[lane] = acc;
+    }
+  };
+
   auto finish_pair = [&]() {
     const bool whole = (seg_first == 0) && (seg_last == cur_np - 1);
     const int slot = gw * 2 + (seg_index == 0 ? 0 : 1);
@@ -394,9 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float2*>(dst + n * 8 + qt * 2) =
                 make_float2(o[mt][n][2 * hb] * inv, o[mt][n][2 * hb + 1] * inv);
           }
-          if (MASS && qt == 0) {
-            a.row_lse[static_cast<int64_t>(cur_pair) * a.R + r] = l > 0.f ? m + fast_log2(l) : kNegInf;
-          }
+          if (MASS && qt == 0) my_lse[r] = l > 0.f ? m + fast_log2(l) : kNegInf;
         } else {
           float* po = a.part_o + (static_cast<int64_t>(slot) * a.R + r) * kHeadDim;
 #pragma unroll
@@ -409,6 +493,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float2(m, l);
           }
         }
+      }
+    }
+    if (whole) {
+      if (MASS && a.page_mass != nullptr) write_mass();
+    } else {
+      // Publish this segment; the last of the pair's segments to arrive merges.
+      const int gwa = share_of(N, cur_start, tw);
+      const int nseg = N >= tw ? share_of(N, cur_start + cur_np - 1, tw) - gwa + 1 : cur_np;
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(a.arrivals + cur_pair, 1) == nseg - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        merge_pair(nseg, gwa);
+        if (MASS && a.page_mass != nullptr) write_mass();
+        if (lane == 0) a.arrivals[cur_pair] = 0;   // ready for the next call
       }
     }
     ++seg_index;
@@ -432,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (m1.x != cur_pair) {
       if (cur_pair >= 0) finish_pair();
       begin_pair(m1.x, m1.y, m1.z, m1.w);
+      cur_start = x0 + k - m1.y;
     }
     seg_last = m1.y;
 
@@ -564,95 +667,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// One CTA per (sequence, KV head) pair: merges the partials of a pair cut by
-// warp-share boundaries, writes zero rows for empty pairs and, for verify
-// with page mass, turns the per-page log-sum-exps into normalised mass.
-template <bool MASS>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnArgs a) {
-  __shared__ int s_np, s_L;
-  __shared__ long long s_start, s_total;
-  __shared__ float s_lse[S3R_MAX_ROWS_PER_KV_HEAD];
-  const int pair = blockIdx.x;
-  const int tid = threadIdx.x;
-  if (tid < 32) {
-    const int c = pair / kPairChunk;
-    const int p = c * kPairChunk + tid;
-    const PairGeom g = p < a.n_pairs ? pair_geom(a, p, false) : PairGeom{0, 0, 0};
-    int incl = g.np;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (tid >= o) incl += t;
-    }
-    if (p == pair) {
-      s_np = g.np;
-      s_L = g.L;
-      s_start = static_cast<long long>(a.chunk_prefix[c]) + incl - g.np;
-      s_total = a.chunk_prefix[a.n_chunks];
-    }
-  }
-  __syncthreads();
-  const int np = s_np;
-  const int64_t X = s_start, N = s_total;
-  const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
-  auto row_off = [&](int r) -> int64_t {
-    const int i = r / a.G, g = r - (r / a.G) * a.G;
-    return ((static_cast<int64_t>(s) * a.T + i) * a.Hq + h * a.G + g) * kHeadDim;
-  };
-
-  if (np == 0) {
-    for (int idx = tid; idx < a.R * kHeadDim; idx += blockDim.x)
-      a.out[row_off(idx / kHeadDim) + idx % kHeadDim] = 0.f;
-    if (MASS && a.page_mass != nullptr)
-      for (int lp = tid; lp < a.mass_stride; lp += blockDim.x)
-        a.page_mass[static_cast<int64_t>(pair) * a.mass_stride + lp] = 0.f;
-    return;
-  }
-  const int tw = a.total_warps;
-  const int gwa = share_of(N, X, tw);
-  const int gwb = share_of(N, X + np - 1, tw);
-  if (gwa == gwb) {
-    if (!MASS) return;
-    if (tid < a.R) s_lse[tid] = a.row_lse[static_cast<int64_t>(pair) * a.R + tid];
-  } else {
-    for (int r = 0; r < a.R; ++r) {
-      float M = kNegInf;
-      for (int gw = gwa; gw <= gwb; ++gw) {
-        const int64_t st = share_start(N, gw, tw);
-        if (gw > gwa && st == share_start(N, gw + 1, tw)) continue;   // empty share
-        const int slot = gw * 2 + ((gw == gwa && st < X) ? 1 : 0);
-        M = fmaxf(M, a.part_ml[(static_cast<int64_t>(slot) * a.R + r) * 2]);
-      }
-      const float Mu = M == kNegInf ? 0.f : M;
-      float lsum = 0.f, acc = 0.f;
-      for (int gw = gwa; gw <= gwb; ++gw) {
-        const int64_t st = share_start(N, gw, tw);
-        if (gw > gwa && st == share_start(N, gw + 1, tw)) continue;
-        const int slot = gw * 2 + ((gw == gwa && st < X) ? 1 : 0);
-        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + r) * 2);
-        const float w = fast_exp2(ml.x - Mu);
-        lsum += ml.y * w;
-        acc += a.part_o[(static_cast<int64_t>(slot) * a.R + r) * kHeadDim + tid] * w;
-      }
-      a.out[row_off(r) + tid] = lsum > 0.f ? acc / lsum : 0.f;
-      if (MASS && tid == 0) s_lse[r] = lsum > 0.f ? M + fast_log2(lsum) : kNegInf;
-    }
-  }
-  if (!MASS || a.page_mass == nullptr) return;
-  __syncthreads();
-  for (int lp = tid; lp < a.mass_stride; lp += blockDim.x) {
-    float mass = 0.f;
-    if (lp < np) {
-      const float* pl = a.page_lse + (static_cast<int64_t>(pair) * a.max_pages + lp) * a.R;
-      for (int r = 0; r < a.R; ++r) {
-        const float v = pl[r];
-        if (v != kNegInf && s_lse[r] != kNegInf) mass += fast_exp2(v - s_lse[r]);
-      }
-    }
-    a.page_mass[static_cast<int64_t>(pair) * a.mass_stride + lp] = mass;
-  }
-}
-
 template <int MT, bool MASS>
 cudaError_t launch_variant(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
                            int grid, cudaStream_t stream) {
@@ -662,9 +676,6 @@ cudaError_t launch_variant(const CUtensorMap& kmap, const CUtensorMap& vmap, con
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   attn_partial_kernel<MT, MASS><<<grid, kThreads, smem, stream>>>(kmap, vmap, a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_combine_kernel<MASS><<<a.n_pairs, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -672,7 +683,7 @@ cudaError_t launch_variant(const CUtensorMap& kmap, const CUtensorMap& vmap, con
 
 size_t attn_smem_bytes(int n_chunks) {
   return 1024 + static_cast<size_t>(kAttnWarps) * kAttnStages * kStageBytes +
-         static_cast<size_t>(kAttnWarps) * kAttnStages * (8 + 32) + 32 * 4 +
+         static_cast<size_t>(kAttnWarps) * kAttnStages * (8 + 32) + 32 * 4 + kAttnWarps * 32 * 4 +
          static_cast<size_t>(n_chunks + 1) * 4;
 }
 
@@ -681,18 +692,15 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 AttnWorkspaceLayout attn_workspace_layout(int n_pairs, int rows, int max_pages, int total_warps,
                                           bool with_mass) {
   AttnWorkspaceLayout L{};
-  const int n_chunks = (n_pairs + kPairChunk - 1) / kPairChunk;
   size_t off = 0;
   L.err_off = off;
   off += 256;
-  L.prefix_off = off;
-  off = align256(off + static_cast<size_t>(n_chunks + 1) * 4);
+  L.arrivals_off = off;
+  off = align256(off + static_cast<size_t>(n_pairs) * 4);
   L.part_o_off = off;
   off = align256(off + static_cast<size_t>(2) * total_warps * rows * kHeadDim * 4);
   L.part_ml_off = off;
   off = align256(off + static_cast<size_t>(2) * total_warps * rows * 2 * 4);
-  L.row_lse_off = off;
-  if (with_mass) off = align256(off + static_cast<size_t>(n_pairs) * rows * 4);
   L.page_lse_off = off;
   if (with_mass) off = align256(off + static_cast<size_t>(n_pairs) * max_pages * rows * 4);
   L.total = off;

@@ -36,10 +36,9 @@ struct AttnArgs {
   int mass_stride;
   // workspace views
   int* err;
-  int* chunk_prefix;                // [n_chunks + 1]
+  int* arrivals;                    // [n_pairs] segments of a cut pair published so far
   float* part_o;                    // [2 * total_warps][R][128]
   float* part_ml;                   // [2 * total_warps][R][2]
-  float* row_lse;                   // [n_pairs][R]             (page mass only)
   float* page_lse;                  // [n_pairs][max_pages][R]  (page mass only)
   int total_warps;
   int n_pairs;
@@ -47,7 +46,7 @@ struct AttnArgs {
 };
 
 struct AttnWorkspaceLayout {
-  size_t err_off, prefix_off, part_o_off, part_ml_off, row_lse_off, page_lse_off, total;
+  size_t err_off, arrivals_off, part_o_off, part_ml_off, page_lse_off, total;
 };
 
 // Byte layout of the attention workspace for the given geometry.
@@ -56,7 +55,8 @@ AttnWorkspaceLayout attn_workspace_layout(int n_pairs, int rows, int max_pages, 
 
 size_t attn_smem_bytes(int n_chunks);
 
-// Enqueue the partial and combine kernels.  `a` must be fully populated.
+// Enqueue the attention kernel.  `a` must be fully populated; the workspace's
+// arrival counters must be zero (every call leaves them zero).
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
                              int grid, cudaStream_t stream);
 

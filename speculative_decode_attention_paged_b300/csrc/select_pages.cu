@@ -8,10 +8,14 @@
 // mass up to B = min(P, max(ceil(budget * P - 1e-9), |mandatory|)) pages,
 // equal mass -> lower page id; emit ascending.
 //
-// One warp per (sequence, KV head): a 4-pass MSB-first radix select (8 bits a
-// pass, warp-private 256-bin histogram in shared memory) finds the K-th
-// largest mass; ties at the threshold are ranked by page id with ballots; the
-// chosen pages are compacted in ascending order with ballots.
+// One warp per (sequence, KV head).  The warp first stages its mass row in
+// shared memory (coalesced loads, several in flight per lane); a 4-pass
+// MSB-first radix select (8 bits a pass, warp-private 256-bin histogram in
+// shared memory) then finds the K-th largest mass; ties at the threshold are
+// ranked by page id with ballots; the chosen pages are compacted in ascending
+// order with ballots.  Every pass after the load reads shared memory only.
+
+#include <algorithm>
 
 #include "s3r_device.cuh"
 
@@ -32,13 +36,15 @@ __global__ void __launch_bounds__(kSelWarps * 32)
                         int n_pairs, int Hkv, int stride, double budget, int n_sink, int n_recent,
                         int32_t* __restrict__ sel_pages, int32_t* __restrict__ sel_count, int b_max,
                         int* err) {
-  __shared__ int hist_all[kSelWarps][256];
+  extern __shared__ int sel_smem[];
+  const int warps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * kSelWarps + warp;
+  const int pair = blockIdx.x * warps + warp;
   if (pair >= n_pairs) return;
-  int* hist = hist_all[warp];
+  int* hist = sel_smem + warp * 256;
+  float* row = reinterpret_cast<float*>(sel_smem + warps * 256) + static_cast<int64_t>(warp) * stride;
   const int s = pair / Hkv;
-  const float* row = mass + static_cast<int64_t>(pair) * stride;
+  const float* grow = mass + static_cast<int64_t>(pair) * stride;
   int32_t* out = sel_pages + static_cast<int64_t>(pair) * b_max;
 
   const int len = __ldg(sel_lens + s);
@@ -50,6 +56,18 @@ __global__ void __launch_bounds__(kSelWarps * 32)
     }
     for (int i = lane; i < b_max; i += 32) out[i] = -1;
     return;
+  }
+  {
+    int pg = lane;
+    for (; pg + 7 * 32 < P; pg += 8 * 32) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldg(grow + pg + j * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) row[pg + j * 32] = v[j];
+    }
+    for (; pg < P; pg += 32) row[pg] = __ldg(grow + pg);
+    __syncwarp();
   }
   const int sink_end = min(n_sink, P);
   const int rec_start = max(P - n_recent, 0);
@@ -76,7 +94,7 @@ __global__ void __launch_bounds__(kSelWarps * 32)
       __syncwarp();
       for (int pg = lane; pg < P; pg += 32) {
         if (mandatory(pg)) continue;
-        const uint32_t key = mass_key(__ldg(row + pg));
+        const uint32_t key = mass_key(row[pg]);
         if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
       }
       __syncwarp();
@@ -128,7 +146,7 @@ __global__ void __launch_bounds__(kSelWarps * 32)
     const int pg = base + lane;
     const bool in = pg < P;
     const bool cand = in && !take_all && K > 0 && !mandatory(pg);
-    const uint32_t key = cand ? mass_key(__ldg(row + pg)) : 0u;
+    const uint32_t key = cand ? mass_key(row[pg]) : 0u;
     bool chosen = in && (take_all || mandatory(pg) || (cand && key > thresh));
     // Keys equal to the threshold: the lowest page ids first.
     const bool is_eq = cand && key == thresh;
@@ -153,10 +171,22 @@ cudaError_t launch_select_pages(const float* mass, const int32_t* sel_lens, int 
                                 cudaStream_t stream) {
   const int n_pairs = S * Hkv;
   if (n_pairs == 0) return cudaSuccess;
-  const int grid = (n_pairs + kSelWarps - 1) / kSelWarps;
-  select_pages_kernel<<<grid, kSelWarps * 32, 0, stream>>>(mass, sel_lens, n_pairs, Hkv, stride,
-                                                            budget, n_sink, n_recent, sel_pages,
-                                                            sel_count, b_max, err);
+  // Warps per CTA: as many as keep (histogram + staged row) per warp within
+  // 96 KB of shared memory, so two CTAs fit on an SM.
+  const size_t per_warp = 256 * sizeof(int) + static_cast<size_t>(stride) * sizeof(float);
+  int warps = static_cast<int>(std::min<size_t>(kSelWarps, std::max<size_t>(1, (96u << 10) / per_warp)));
+  const size_t smem = per_warp * warps;
+  if (smem > (200u << 10)) return cudaErrorInvalidValue;
+  if (smem > (48u << 10)) {
+    const cudaError_t e = cudaFuncSetAttribute(select_pages_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  const int grid = (n_pairs + warps - 1) / warps;
+  select_pages_kernel<<<grid, warps * 32, smem, stream>>>(mass, sel_lens, n_pairs, Hkv, stride, budget,
+                                                          n_sink, n_recent, sel_pages, sel_count, b_max,
+                                                          err);
   return cudaGetLastError();
 }
 
