@@ -76,6 +76,32 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int kv_heads, int64_t n
   return r == CUDA_SUCCESS;
 }
 
+// 4-D view of the verify queries q [S][T][Hq][128] bf16: box (64, G, T, 1)
+// = one 64-column half of the T x G query rows of one (sequence, KV head).
+bool encode_query_map(CUtensorMap* map, const void* q, int S, int T, int Hq, int G) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hq),
+                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(S)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                           static_cast<cuuint64_t>(Hq) * kHeadDim * 2,
+                           static_cast<cuuint64_t>(T) * Hq * kHeadDim * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(T), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Largest dynamic shared memory a block may opt into on the current device.
+size_t max_dynamic_smem() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  return static_cast<size_t>(v);
+}
+
 s3r_status validate_kv(const s3r_paged_kv* kv) {
   if (kv == nullptr) return S3R_ERR_INVALID_ARG;
   if (kv->head_dim != kHeadDim || kv->page_size != kPage) return S3R_ERR_UNSUPPORTED;
@@ -165,6 +191,15 @@ s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, 
   a.total_warps = total_warps;
   a.n_pairs = n_pairs;
   a.n_chunks = (n_pairs + kPairChunk - 1) / kPairChunk;
+  // Verify with more than 16 query rows per KV head runs on the tcgen05
+  // kernel (the CUDA-core kernel would hold two 16-row MMA tiles per warp and
+  // spill); up to 16 rows the CUDA-core kernel streams at the copy bandwidth.
+  if (mode == kModeVerify && R > 16 && R <= S3R_MAX_ROWS_PER_KV_HEAD &&
+      verify_tc_smem_bytes(a.n_chunks) <= max_dynamic_smem()) {
+    CUtensorMap qmap;
+    if (!encode_query_map(&qmap, q, kv->num_seqs, T, kv->num_q_heads, G)) return S3R_ERR_CUDA;
+    return to_status(launch_verify_tc(kmap, vmap, qmap, a, sms, static_cast<cudaStream_t>(stream)));
+  }
   return to_status(launch_attention(kmap, vmap, a, sms, static_cast<cudaStream_t>(stream)));
 }
 

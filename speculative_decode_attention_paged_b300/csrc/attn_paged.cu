@@ -33,6 +33,7 @@
 //   * Data-dependent errors (bad page id, bad length) skip the page and set a
 //     bit in the device error word; every wait is bounded.
 
+#include "attn_common.cuh"
 #include "attn_paged.cuh"
 #include "s3r_device.cuh"
 
@@ -40,175 +41,10 @@ namespace s3r {
 
 namespace {
 
+using namespace attn;
+
 constexpr int kStageBytes = 2 * kTileBytes;   // K tile + V tile
 constexpr int kThreads = kAttnWarps * 32;
-constexpr float kNegInf = -__builtin_huge_valf();
-
-struct PairGeom {
-  int np;     // pages in the pair's stream
-  int L;      // ctx_len (dense) or hist_len (sparse / verify)
-  int cnt;    // selected pages (sparse)
-};
-
-// Pages of pair `pair` in the global stream, with its length and selection count.
-__device__ PairGeom pair_geom(const AttnArgs& a, int pair, bool report) {
-  PairGeom g{0, 0, 0};
-  const int s = pair / a.Hkv;
-  const int len = __ldg(a.lens + s);
-  const int cap = a.max_pages * kPage;
-  if (a.mode == kModeDense) {
-    if (len < 0 || len > cap) {
-      if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
-      return g;
-    }
-    g.L = len;
-    g.np = (len + kPage - 1) / kPage;
-  } else if (a.mode == kModeVerify) {
-    if (len < 0 || len + a.T > cap) {
-      if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
-      return g;
-    }
-    g.L = len;
-    g.np = (len + a.T + kPage - 1) / kPage;
-  } else {
-    const int last = len + a.draft_pos;
-    if (len < 0 || last >= cap) {
-      if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
-      return g;
-    }
-    int cnt = __ldg(a.sel_count + pair);
-    if (cnt < 0 || cnt > a.b_max) {
-      if (report) report_error(a.err, S3R_DEVERR_BAD_COUNT);
-      cnt = 0;
-    }
-    g.L = len;
-    g.cnt = cnt;
-    g.np = cnt + (last / kPage - len / kPage + 1);
-  }
-  return g;
-}
-
-struct Entry {
-  int lp;     // logical page
-  int lo;     // first visible token (absolute)
-  int hi;     // one past the last visible token
-  int phys;   // physical page, -1 = nothing to load
-};
-
-// Entry e of pair `pair`'s page stream.
-__device__ Entry pair_entry(const AttnArgs& a, int pair, const PairGeom& g, int e) {
-  Entry r{-1, 0, 0, -1};
-  const int s = pair / a.Hkv;
-  if (a.mode == kModeDense) {
-    r.lp = e;
-    r.lo = e * kPage;
-    r.hi = min(r.lo + kPage, g.L);
-  } else if (a.mode == kModeVerify) {
-    r.lp = e;
-    r.lo = e * kPage;
-    r.hi = min(r.lo + kPage, g.L + a.T);
-  } else if (e < g.cnt) {
-    const int lp = __ldg(a.sel_pages + static_cast<int64_t>(pair) * a.b_max + e);
-    if (lp < 0 || lp >= a.max_pages) {
-      report_error(a.err, S3R_DEVERR_BAD_PAGE);
-      return r;
-    }
-    r.lp = lp;
-    r.lo = lp * kPage;
-    r.hi = min(r.lo + kPage, g.L);
-  } else {
-    r.lp = g.L / kPage + (e - g.cnt);
-    r.lo = max(r.lp * kPage, g.L);
-    r.hi = min(r.lp * kPage + kPage, g.L + a.draft_pos + 1);
-  }
-  if (r.lo < r.hi) {
-    const int phys = __ldg(a.block_table + static_cast<int64_t>(s) * a.max_pages + r.lp);
-    if (phys < 0 || static_cast<int64_t>(phys) >= a.num_phys_pages) {
-      report_error(a.err, S3R_DEVERR_BAD_PAGE);
-    } else {
-      r.phys = phys;
-    }
-  }
-  return r;
-}
-
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float quad_max(float v) {
-  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-}
-
-__device__ __forceinline__ float quad_sum(float v) {
-  v += __shfl_xor_sync(0xffffffffu, v, 1);
-  return v + __shfl_xor_sync(0xffffffffu, v, 2);
-}
-
-// Global page index where warp share `gw` starts (shares split N pages evenly).
-__device__ __forceinline__ int64_t share_start(int64_t N, int gw, int tw) {
-  return N * gw / tw;
-}
-
-// The warp share holding global page x (the last share whose start is <= x).
-__device__ __forceinline__ int share_of(int64_t N, int64_t x, int tw) {
-  return static_cast<int>(((x + 1) * tw - 1) / N);
-}
-
-// In-CTA exclusive scan of vals[0..n) in place; vals[n] receives the total.
-__device__ void block_exclusive_scan(int* vals, int n, int* scratch) {
-  const int tid = threadIdx.x;
-  const int per = (n + kThreads - 1) / kThreads;
-  const int b = min(tid * per, n), e = min(b + per, n);
-  int local = 0;
-  for (int i = b; i < e; ++i) local += vals[i];
-  // warp inclusive scan of the thread sums
-  const int lane = tid & 31, warp = tid >> 5;
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kAttnWarps ? scratch[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += t;
-    }
-    if (lane < kAttnWarps) scratch[lane] = w;   // inclusive warp totals
-  }
-  __syncthreads();
-  int run = incl - local + (warp > 0 ? scratch[warp - 1] : 0);
-  for (int i = b; i < e; ++i) {
-    const int v = vals[i];
-    vals[i] = run;
-    run += v;
-  }
-  if (tid == kThreads - 1) vals[n] = run;
-  __syncthreads();
-}
-
-// Zero output rows (and zero page mass) of a pair with no page to read.
-__device__ void zero_pair(const AttnArgs& a, int pair) {
-  const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
-  for (int r = 0; r < a.R; ++r) {
-    const int i = r / a.G, g = r - (r / a.G) * a.G;
-    float4* dst = reinterpret_cast<float4*>(
-        a.out + ((static_cast<int64_t>(s) * a.T + i) * a.Hq + h * a.G + g) * kHeadDim);
-    for (int c = 0; c < kHeadDim / 4; ++c) dst[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (a.page_mass != nullptr) {
-    float* m = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
-    for (int lp = 0; lp < a.mass_stride; ++lp) m[lp] = 0.f;
-  }
-}
 
 // Smem address of the 16-byte chunk holding (token, d0..d0+7) of a swizzled
 // K or V tile: two 64-column halves of 16 rows x 128 B, 128B-swizzled.
@@ -252,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   fence_barrier_init();
   __syncthreads();
-  block_exclusive_scan(prefix, a.n_chunks, scratch);
+  block_exclusive_scan<kThreads>(prefix, a.n_chunks, scratch);
 
   const int64_t N = prefix[a.n_chunks];
   const int tw = a.total_warps;

@@ -60,4 +60,11 @@ size_t attn_smem_bytes(int n_chunks);
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnArgs& a,
                              int grid, cudaStream_t stream);
 
+// Verify on tcgen05 (rows per KV head <= 32): dynamic shared memory it needs
+// for `n_chunks` chunks of 32 pairs, and the launch (qmap: 4-D view of the
+// queries [S][T][Hq][128], box (64, G, T, 1), 128-byte swizzle).
+size_t verify_tc_smem_bytes(int n_chunks);
+cudaError_t launch_verify_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                             const AttnArgs& a, int grid, cudaStream_t stream);
+
 }  // namespace s3r
