@@ -166,6 +166,31 @@ __device__ void block_exclusive_scan(int* vals, int n, int* scratch) {
   __syncthreads();
 }
 
+// Normalised mass of one page: sum over rows r < R of 2^(lse_page[r] - LSE[r]).
+// lse_page is 16-byte aligned when R is a multiple of 4.
+__device__ __forceinline__ float page_mass_of(const float* lse_page, const float* row_lse, int R) {
+  float mass = 0.f;
+  if ((R & 3) == 0) {
+#pragma unroll 8
+    for (int r = 0; r < R; r += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(lse_page + r));
+      const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float L = row_lse[r + k];
+        if (e[k] != kNegInf && L != kNegInf) mass += fast_exp2(e[k] - L);
+      }
+    }
+  } else {
+    for (int r = 0; r < R; ++r) {
+      const float v = __ldcg(lse_page + r);
+      const float L = row_lse[r];
+      if (v != kNegInf && L != kNegInf) mass += fast_exp2(v - L);
+    }
+  }
+  return mass;
+}
+
 // Zero output rows (and zero page mass) of a pair with no page to read.
 __device__ void zero_pair(const AttnArgs& a, int pair) {
   const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;

@@ -238,18 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     float* dst = a.page_mass + static_cast<int64_t>(cur_pair) * a.mass_stride;
     const float* pl = a.page_lse + static_cast<int64_t>(cur_pair) * a.max_pages * a.R;
-    for (int lp = lane; lp < a.mass_stride; lp += 32) {
-      float mass = 0.f;
-      if (lp < cur_np) {
-        const float* e = pl + static_cast<int64_t>(lp) * a.R;
-        for (int r = 0; r < a.R; ++r) {
-          const float v = __ldcg(e + r);
-          const float L = my_lse[r];
-          if (v != kNegInf && L != kNegInf) mass += fast_exp2(v - L);
-        }
-      }
-      dst[lp] = mass;
-    }
+    for (int lp = lane; lp < a.mass_stride; lp += 32)
+      dst[lp] = lp < cur_np ? page_mass_of(pl + static_cast<int64_t>(lp) * a.R, my_lse, a.R) : 0.f;
   };
 
   // Slot of segment j of a pair cut by warp shares: the pair's pages start at

@@ -23,9 +23,10 @@
 //     32-column halves of O^T are added at the end.  (An MMA costs at least
 //     ~61 cycles whatever its N up to 128, so fewer, wider MMAs pay.)
 //   * Warp roles: warp 0 = TMA producer (3 stages of 8 pages of K and V),
-//     warp 1 = MMA issuer (one thread) and TMEM owner, warps 2-5 = softmax: a
-//     thread owns one token of the tile (one TMEM lane) and the 32 rows; row
-//     maxima and sums are reduced with butterfly reduce-scatters.  The running
+//     warp 1 = MMA issuer (one thread) and TMEM owner, warps 2-9 = softmax in
+//     two warpgroups of 16 query rows each: a thread owns one token of the
+//     tile (one TMEM lane) and its group's 16 rows; row maxima and sums are
+//     reduced with butterfly reduce-scatters.  The running
 //     max is refreshed only when a tile's max exceeds it by more than 2^8
 //     (then O^T is rescaled in TMEM); otherwise p <= 256 and the stale max is
 //     exact to use.  Accumulators: S^T double-buffered and O^T in TMEM.
@@ -53,9 +54,12 @@ constexpr int kTcStageBytes = 4 * kTcRegion;           // K lo, K hi, V lo, V hi
 constexpr int kTcRows = 32;                            // MMA N: query rows per KV head
 constexpr int kTcQHalf = kTcRows * 128;                // 4 KiB: 32 rows x 64 columns
 constexpr int kTcPBytes = 128 * 2 * kTcRows * 2;       // 16 KiB of bf16 P^T: high part | remainder
-constexpr int kTcThreads = 192;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kSoftmaxBar = 1;                         // named barrier of the softmax warps
+constexpr int kTcThreads = 320;                        // producer, MMA, 2 x 4 softmax warps
+constexpr int kSoftmaxThreads = 256;
+constexpr int kWgThreads = 128;
+constexpr int kRowsWg = 16;                            // query rows per softmax warpgroup
+constexpr int kWgBar0 = 1;                             // named barriers 1, 2: one per warpgroup
+constexpr int kAllBar = 3;                             // named barrier 3: both warpgroups
 constexpr uint32_t kTmemCols = 128;                    // S^T x 2 (32 columns each), O^T (64)
 constexpr uint32_t kColS = 0, kColO = 64;              // O^T: 32 columns from P high, 32 from P low
 constexpr float kRescaleSlack = 8.f;
@@ -81,8 +85,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int n_chunks) {
   s.p = off;       off += kTcPBytes;
   s.meta = off;    off += kTcStages * sizeof(TileMeta);
   s.bars = off;    off += 16 * sizeof(uint64_t);
-  s.red_max = off; off += 2 * 4 * 32 * sizeof(float);
-  s.red_sum = off; off += 4 * 32 * sizeof(float);
+  s.red_max = off; off += 2 * 2 * 4 * 16 * sizeof(float);   // [group][buffer][quarter][row]
+  s.red_sum = off; off += 2 * 4 * 16 * sizeof(float);       // [group][quarter][row]
   s.rowbuf = off;  off += 3 * 32 * sizeof(float);   // row LSE, row max, row 1/sum
   s.misc = off;    off += 4 * sizeof(int);          // TMEM base, abort flag, last-arrival flag
   s.scratch = off; off += 32 * sizeof(int);
@@ -103,15 +107,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-// Butterfly reduce-scatter of v[32] over groups of WIDTH lanes: afterwards
-// v[0 .. 32/WIDTH) holds the group's reduction of rows base .. base+32/WIDTH-1,
-// base = (lane % WIDTH) * (32 / WIDTH).  Fixed order: deterministic.
-template <int WIDTH, bool MAX>
-__device__ __forceinline__ void reduce_scatter(float (&v)[32], int lane) {
+// Butterfly reduce-scatter of v[VALS] over groups of WIDTH lanes (VALS <=
+// WIDTH, both powers of two): afterwards v[0] holds the group's reduction of
+// row (lane % WIDTH) / (WIDTH / VALS).  Fixed order: deterministic.
+template <int WIDTH, int VALS, bool MAX>
+__device__ __forceinline__ void reduce_scatter(float (&v)[VALS], int lane) {
 #pragma unroll
-  for (int step = 0; (WIDTH >> (step + 1)) >= 1; ++step) {
+  for (int step = 0; (VALS >> (step + 1)) >= 1; ++step) {
     const int off = WIDTH >> (step + 1);
-    const int n = 16 >> step;
+    const int n = VALS >> (step + 1);
     const bool up = (lane & off) != 0;
 #pragma unroll
     for (int j = 0; j < n; ++j) {
@@ -120,6 +124,11 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[32], int lane) {
       const float recv = __shfl_xor_sync(0xffffffffu, send, off);
       v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
     }
+  }
+#pragma unroll
+  for (int off = WIDTH / VALS / 2; off >= 1; off >>= 1) {
+    const float recv = __shfl_xor_sync(0xffffffffu, v[0], off);
+    v[0] = MAX ? fmaxf(v[0], recv) : v[0] + recv;
   }
 }
 
@@ -151,8 +160,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* p_full = bars + 12;
   uint64_t* o_done = bars + 13;
   uint64_t* drain = bars + 14;
-  float* red_max = reinterpret_cast<float*>(smem + L.red_max);   // [2][4][32]
-  float* red_sum = reinterpret_cast<float*>(smem + L.red_sum);   // [4][32]
+  float* red_max = reinterpret_cast<float*>(smem + L.red_max);
+  float* red_sum = reinterpret_cast<float*>(smem + L.red_sum);
   float* row_lse = reinterpret_cast<float*>(smem + L.rowbuf);    // [32]
   float* row_max = row_lse + 32;
   float* row_inv = row_lse + 64;
@@ -175,9 +184,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 4);
+      mbar_init(&s_free[b], 8);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -423,16 +432,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else {
-    // =========================== softmax warps (128 threads)
+    // =========================== softmax: two warpgroups of 4 warps, 16 rows each
+    const int wg = (warp - 2) >> 2;                // warpgroup: rows wg*16 .. wg*16+15
+    const int r0 = wg * kRowsWg;
     const int q4 = warp & 3;                       // TMEM lane quarter this warp may access
     const int i = q4 * 32 + lane;                  // token slot of the tile = TMEM lane
-    const int st_tid = tid - 64;                   // 0..127
+    const int sm_tid = tid - 64;                   // 0..255 over both warpgroups
+    const int wg_bar = kWgBar0 + wg;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    float m_run[32], l_part[32];
+    float* rmax = red_max + wg * 128;              // [2 buffers][4 quarters][16 rows]
+    float* rsum = red_sum + wg * 64;               // [4 quarters][16 rows]
+    float m_run[kRowsWg], l_part[kRowsWg];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-      m_run[r] = kNegInf;
-      l_part[r] = 0.f;
+    for (int j = 0; j < kRowsWg; ++j) {
+      m_run[j] = kNegInf;
+      l_part[j] = 0.f;
     }
     int seg_index = 0;
     for (int t = 0;; ++t) {
@@ -443,7 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int flags = ok ? m.flags : kTileEnd;
       if (ok && !(flags & kTileEnd))
         ok = wait_or_abort(&s_full[b], static_cast<uint32_t>((t >> 1) & 1), abort_flag, a.err);
-      if (!named_bar_and(kSoftmaxBar, kSoftmaxThreads, ok)) break;
+      if (!named_bar_and(kAllBar, kSoftmaxThreads, ok)) break;
       if (flags & kTileEnd) break;
       const int pair = m.pair, e0 = m.e0, n = m.n, np = m.np, Lh = m.L;
       const int page = i >> 4;
@@ -452,14 +466,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const long long pstart = m.start;
       if (flags & kTileFirst) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          m_run[r] = kNegInf;
-          l_part[r] = 0.f;
+        for (int j = 0; j < kRowsWg; ++j) {
+          m_run[j] = kNegInf;
+          l_part[j] = 0.f;
         }
       }
       tc_fence_after_sync();
-      float x[32];
-      tmem_ld32(lane_addr + kColS + 32u * b, x);
+      float x[kRowsWg];
+      tmem_ld16(lane_addr + kColS + 32u * b + r0, x);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[b]);
@@ -469,92 +483,91 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool tok = pos >= lo && pos < hi;
       const int r_min = pos <= Lh ? 0 : (pos - Lh) * a.G;
 #pragma unroll
-      for (int r = 0; r < 32; ++r)
-        x[r] = (tok && r >= r_min && r < a.R) ? x[r] * a.scale_log2 : kNegInf;
+      for (int j = 0; j < kRowsWg; ++j) {
+        const int r = r0 + j;
+        x[j] = (tok && r >= r_min && r < a.R) ? x[j] * a.scale_log2 : kNegInf;
+      }
 
       // The running max only moves when some score exceeds it by more than
       // the slack: one vote decides whether this tile needs the exact max.
-      float v[32];
+      float v[kRowsWg];
       bool exceed = false;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) exceed |= x[r] > m_run[r] + kRescaleSlack;
-      const bool need = named_bar_or(kSoftmaxBar, kSoftmaxThreads, exceed);
+      for (int j = 0; j < kRowsWg; ++j) exceed |= x[j] > m_run[j] + kRescaleSlack;
+      bool ok_acc = true;
       bool waited_prev = false;
-      if (need) {
-        // exact tile max per row
+      if (named_bar_or(wg_bar, kWgThreads, exceed)) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) v[r] = x[r];
-        reduce_scatter<32, true>(v, lane);
-        float* rm = red_max + (t & 1) * 128;
-        rm[q4 * 32 + lane] = v[0];
-        named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
-        const float tmax_l = fmaxf(fmaxf(rm[lane], rm[32 + lane]), fmaxf(rm[64 + lane], rm[96 + lane]));
-        float tm[32];
+        for (int j = 0; j < kRowsWg; ++j) v[j] = x[j];
+        reduce_scatter<32, kRowsWg, true>(v, lane);   // lanes 2j, 2j+1: row j of this warp
+        float* rm = rmax + (t & 1) * 64;
+        if ((lane & 1) == 0) rm[q4 * 16 + (lane >> 1)] = v[0];
+        named_bar_sync(wg_bar, kWgThreads);
+        const int jr = lane >> 1;
+        const float tmax_l = fmaxf(fmaxf(rm[jr], rm[16 + jr]), fmaxf(rm[32 + jr], rm[48 + jr]));
+        float alpha[kRowsWg];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) tm[r] = __shfl_sync(0xffffffffu, tmax_l, r);
-        float alpha[32];
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const float mn = fmaxf(m_run[r], tm[r]);
-          alpha[r] = mn == kNegInf ? 1.f : (m_run[r] == kNegInf ? 0.f : fast_exp2(m_run[r] - mn));
-          m_run[r] = mn;
-          l_part[r] *= alpha[r];
+        for (int j = 0; j < kRowsWg; ++j) {
+          const float tm = __shfl_sync(0xffffffffu, tmax_l, 2 * j);
+          const float mn = fmaxf(m_run[j], tm);
+          alpha[j] = mn == kNegInf ? 1.f : (m_run[j] == kNegInf ? 0.f : fast_exp2(m_run[j] - mn));
+          m_run[j] = mn;
+          l_part[j] *= alpha[j];
         }
         if (!(flags & kTileFirst)) {
-          // O^T holds this pair's earlier tiles: rescale it once PV(t-1) is done
-          ok = wait_or_abort(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag, a.err);
-          if (!named_bar_and(kSoftmaxBar, kSoftmaxThreads, ok)) break;
-          tc_fence_after_sync();
-          float o[32];
-          tmem_ld32(lane_addr + kColO, o);
+          // O^T holds this pair's earlier tiles: rescale this group's columns once PV(t-1) is done
+          const bool okw = wait_or_abort(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag, a.err);
+          if (named_bar_and(wg_bar, kWgThreads, okw)) {
+            tc_fence_after_sync();
+            float o[kRowsWg];
+            tmem_ld16(lane_addr + kColO + r0, o);
 #pragma unroll
-          for (int r = 0; r < 32; ++r) o[r] *= alpha[r];
-          tmem_st32(lane_addr + kColO, o);
-          tmem_ld32(lane_addr + kColO + 32, o);
+            for (int j = 0; j < kRowsWg; ++j) o[j] *= alpha[j];
+            tmem_st16(lane_addr + kColO + r0, o);
+            tmem_ld16(lane_addr + kColO + 32 + r0, o);
 #pragma unroll
-          for (int r = 0; r < 32; ++r) o[r] *= alpha[r];
-          tmem_st32(lane_addr + kColO + 32, o);
-          tc_fence_before_sync();
+            for (int j = 0; j < kRowsWg; ++j) o[j] *= alpha[j];
+            tmem_st16(lane_addr + kColO + 32 + r0, o);
+            tc_fence_before_sync();
+          } else {
+            ok_acc = false;
+          }
           waited_prev = true;
         }
       }
-      float mu[32];
-      float m_lane = 0.f;
+      float mu[kRowsWg];
+      float m_lane = 0.f;   // m_use of row (lane & 15) of this group
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        mu[r] = m_run[r] == kNegInf ? 0.f : m_run[r];
-        if (r == lane) m_lane = mu[r];
+      for (int j = 0; j < kRowsWg; ++j) {
+        mu[j] = m_run[j] == kNegInf ? 0.f : m_run[j];
+        if (j == (lane & 15)) m_lane = mu[j];
       }
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        x[r] = fast_exp2(x[r] - mu[r]);
-        l_part[r] += x[r];
+      for (int j = 0; j < kRowsWg; ++j) {
+        x[j] = fast_exp2(x[j] - mu[j]);
+        l_part[j] += x[j];
       }
       if (MASS) {
         // per (page, row) log-sum-exp: sum over the 16 tokens of the page
 #pragma unroll
-        for (int r = 0; r < 32; ++r) v[r] = x[r];
-        reduce_scatter<16, false>(v, lane);
-        const int r0 = 2 * (lane & 15);
-        const float m0 = __shfl_sync(0xffffffffu, m_lane, r0);
-        const float m1 = __shfl_sync(0xffffffffu, m_lane, r0 + 1);
-        if (page < n) {
-          float* pl = a.page_lse + (static_cast<int64_t>(pair) * a.max_pages + e0 + page) * a.R;
-          if (r0 < a.R) pl[r0] = v[0] > 0.f ? m0 + fast_log2(v[0]) : kNegInf;
-          if (r0 + 1 < a.R) pl[r0 + 1] = v[1] > 0.f ? m1 + fast_log2(v[1]) : kNegInf;
+        for (int j = 0; j < kRowsWg; ++j) v[j] = x[j];
+        reduce_scatter<16, kRowsWg, false>(v, lane);   // lane holds row (lane & 15)
+        const int r = r0 + (lane & 15);
+        if (page < n && r < a.R) {
+          a.page_lse[(static_cast<int64_t>(pair) * a.max_pages + e0 + page) * a.R + r] =
+              v[0] > 0.f ? m_lane + fast_log2(v[0]) : kNegInf;
         }
       }
       // P^T (bf16 high part and remainder); the buffer is free once PV(t-1) is done
-      if (t > 0 && !waited_prev) {
-        ok = wait_or_abort(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag, a.err);
-        if (!named_bar_and(kSoftmaxBar, kSoftmaxThreads, ok)) break;
-      }
+      if (t > 0 && !waited_prev)
+        ok_acc = ok_acc && wait_or_abort(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag, a.err);
+      if (!named_bar_and(kAllBar, kSoftmaxThreads, ok_acc)) break;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t h4[4], l4[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) split_bf16x2(x[c * 8 + 2 * j], x[c * 8 + 2 * j + 1], h4[j], l4[j]);
-        const int off = (i >> 3) * 1024 + c * 128 + (i & 7) * 16;
+        for (int jj = 0; jj < 4; ++jj) split_bf16x2(x[c * 8 + 2 * jj], x[c * 8 + 2 * jj + 1], h4[jj], l4[jj]);
+        const int off = (i >> 3) * 1024 + (2 * wg + c) * 128 + (i & 7) * 16;
         *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(h4[0], h4[1], h4[2], h4[3]);
         *reinterpret_cast<uint4*>(pbuf + off + 4 * 128) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
       }
@@ -566,55 +579,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!(flags & kTileLast)) continue;
       // =========================== end of this pair's segment
       ok = wait_or_abort(o_done, static_cast<uint32_t>(t & 1), abort_flag, a.err);
-      if (!named_bar_and(kSoftmaxBar, kSoftmaxThreads, ok)) break;
+      if (!named_bar_and(kAllBar, kSoftmaxThreads, ok)) break;
       tc_fence_after_sync();
-      float o[32];
-      tmem_ld32(lane_addr + kColO, o);          // thread i holds column d = i of every row
-      tmem_ld32(lane_addr + kColO + 32, v);     // the P-remainder half
+      float o[kRowsWg];
+      tmem_ld16(lane_addr + kColO + r0, o);       // thread i holds column d = i of the group's rows
+      tmem_ld16(lane_addr + kColO + 32 + r0, v);  // the P-remainder half
 #pragma unroll
-      for (int r = 0; r < 32; ++r) o[r] += v[r];
+      for (int j = 0; j < kRowsWg; ++j) o[j] += v[j];
       tc_fence_before_sync();
 #pragma unroll
-      for (int r = 0; r < 32; ++r) v[r] = l_part[r];
-      reduce_scatter<32, false>(v, lane);
-      red_sum[q4 * 32 + lane] = v[0];
-      named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
-      const float L_l = (red_sum[lane] + red_sum[32 + lane]) + (red_sum[64 + lane] + red_sum[96 + lane]);
+      for (int j = 0; j < kRowsWg; ++j) v[j] = l_part[j];
+      reduce_scatter<32, kRowsWg, false>(v, lane);
+      if ((lane & 1) == 0) rsum[q4 * 16 + (lane >> 1)] = v[0];
+      named_bar_sync(wg_bar, kWgThreads);
+      const int jr = lane >> 1;                    // lanes 2j, 2j+1: row r0 + j
+      const float L_l = (rsum[jr] + rsum[16 + jr]) + (rsum[32 + jr] + rsum[48 + jr]);
+      float m_jr = 0.f;
+#pragma unroll
+      for (int j = 0; j < kRowsWg; ++j)
+        if (j == jr) m_jr = mu[j];
       const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
+      int last = 0;
       if (flags & kTileWhole) {
         const float inv_l = L_l > 0.f ? 1.f / L_l : 0.f;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const float ir = __shfl_sync(0xffffffffu, inv_l, r);
-          if (r < a.R) a.out[q_row_off(a, s, h, r) + i] = o[r] * ir;
+        for (int j = 0; j < kRowsWg; ++j) {
+          const float ir = __shfl_sync(0xffffffffu, inv_l, 2 * j);
+          if (r0 + j < a.R) a.out[q_row_off(a, s, h, r0 + j) + i] = o[j] * ir;
         }
-        if (MASS && q4 == 0) row_lse[lane] = L_l > 0.f ? m_lane + fast_log2(L_l) : kNegInf;
+        if (MASS && q4 == 0 && (lane & 1) == 0) row_lse[r0 + jr] = L_l > 0.f ? m_jr + fast_log2(L_l) : kNegInf;
       } else {
         const int slot = cta * 2 + (seg_index == 0 ? 0 : 1);
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          if (r < a.R) a.part_o[(static_cast<int64_t>(slot) * a.R + r) * kHeadDim + i] = o[r];
-        if (q4 == 0 && lane < a.R)
-          *reinterpret_cast<float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + lane) * 2) =
-              make_float2(m_lane, L_l);
+        for (int j = 0; j < kRowsWg; ++j)
+          if (r0 + j < a.R) a.part_o[(static_cast<int64_t>(slot) * a.R + r0 + j) * kHeadDim + i] = o[j];
+        if (q4 == 0 && (lane & 1) == 0 && r0 + jr < a.R)
+          *reinterpret_cast<float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + r0 + jr) * 2) =
+              make_float2(m_jr, L_l);
         __threadfence();
-        named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
+        named_bar_sync(kAllBar, kSoftmaxThreads);
         const int gwa = share_of(N, pstart, tw);
         const int nseg = N >= tw ? share_of(N, pstart + np - 1, tw) - gwa + 1 : np;
-        if (st_tid == 0) *last_flag = atomicAdd(a.arrivals + pair, 1) == nseg - 1;
-        named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
-        if (*last_flag) {
+        if (sm_tid == 0) *last_flag = atomicAdd(a.arrivals + pair, 1) == nseg - 1;
+        named_bar_sync(kAllBar, kSoftmaxThreads);
+        last = *last_flag;
+        if (last) {
           __threadfence();
           auto slot_of = [&](int j) -> int {
             if (N >= tw) return (gwa + j) * 2 + ((j == 0 && share_start(N, gwa, tw) < pstart) ? 1 : 0);
             return share_of(N, pstart + j, tw) * 2;
           };
-          if (q4 == 0) {
+          if (q4 == 0 && lane < kRowsWg) {
             float M = kNegInf, Ls = 0.f;
-            if (lane < a.R) {
+            if (r0 + lane < a.R) {
               for (int j = 0; j < nseg; ++j) {
                 const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-                    a.part_ml + (static_cast<int64_t>(slot_of(j)) * a.R + lane) * 2));
+                    a.part_ml + (static_cast<int64_t>(slot_of(j)) * a.R + r0 + lane) * 2));
                 if (ml.y > 0.f) {
                   const float mn = fmaxf(M, ml.x);
                   Ls = Ls * fast_exp2(M - mn) + ml.y * fast_exp2(ml.x - mn);
@@ -622,44 +642,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
               }
             }
-            row_max[lane] = M;
-            row_inv[lane] = Ls > 0.f ? 1.f / Ls : 0.f;
-            row_lse[lane] = Ls > 0.f ? M + fast_log2(Ls) : kNegInf;
+            row_max[r0 + lane] = M;
+            row_inv[r0 + lane] = Ls > 0.f ? 1.f / Ls : 0.f;
+            row_lse[r0 + lane] = Ls > 0.f ? M + fast_log2(Ls) : kNegInf;
           }
-          named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
-          for (int r = 0; r < a.R; ++r) {
+          named_bar_sync(wg_bar, kWgThreads);
+          for (int j = 0; j < kRowsWg && r0 + j < a.R; ++j) {
+            const int r = r0 + j;
             const float Mr = row_max[r], ir = row_inv[r];
             float acc = 0.f;
-            for (int j = 0; j < nseg; ++j) {
-              const int64_t row = static_cast<int64_t>(slot_of(j)) * a.R + r;
+            for (int sg = 0; sg < nseg; ++sg) {
+              const int64_t row = static_cast<int64_t>(slot_of(sg)) * a.R + r;
               const float mr = __ldcg(a.part_ml + row * 2);
               const float w = mr == kNegInf ? 0.f : fast_exp2(mr - Mr) * ir;
               acc += w * __ldcg(a.part_o + row * kHeadDim + i);
             }
             a.out[q_row_off(a, s, h, r) + i] = acc;
           }
-          if (st_tid == 0) a.arrivals[pair] = 0;
+          if (sm_tid == 0) a.arrivals[pair] = 0;
         }
       }
-      if (MASS && ((flags & kTileWhole) || *last_flag)) {
-        named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      if (MASS && ((flags & kTileWhole) || last)) {
+        named_bar_sync(kAllBar, kSoftmaxThreads);
         float* dst = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
         const float* plse = a.page_lse + static_cast<int64_t>(pair) * a.max_pages * a.R;
-        for (int lp = st_tid; lp < a.mass_stride; lp += kSoftmaxThreads) {
-          float mass = 0.f;
-          if (lp < np) {
-            const float* e = plse + static_cast<int64_t>(lp) * a.R;
-            for (int r = 0; r < a.R; ++r) {
-              const float vv = __ldcg(e + r);
-              const float Lr = row_lse[r];
-              if (vv != kNegInf && Lr != kNegInf) mass += fast_exp2(vv - Lr);
-            }
-          }
-          dst[lp] = mass;
-        }
+        for (int lp = sm_tid; lp < a.mass_stride; lp += kSoftmaxThreads)
+          dst[lp] = lp < np ? page_mass_of(plse + static_cast<int64_t>(lp) * a.R, row_lse, a.R) : 0.f;
       }
       ++seg_index;
-      named_bar_sync(kSoftmaxBar, kSoftmaxThreads);
+      named_bar_sync(kAllBar, kSoftmaxThreads);
     }
   }
 
