@@ -22,7 +22,8 @@
 //     32 rows twice), so one MMA per page carries ~16 bits of P and the two
 //     32-column halves of O^T are added at the end.  (An MMA costs at least
 //     ~61 cycles whatever its N up to 128, so fewer, wider MMAs pay.)
-//   * Warp roles: warp 0 = TMA producer (3 stages of 8 pages of K and V),
+//   * Warp roles: warps 0, 10, 11 = TMA producers (3 stages of 8 pages of K
+//     and V; a tile's page boxes are spread over the three warps),
 //     warp 1 = MMA issuer (one thread) and TMEM owner, warps 2-9 = softmax in
 //     two warpgroups of 16 query rows each: a thread owns one token of the
 //     tile (one TMEM lane) and its group's 16 rows; row maxima and sums are
@@ -54,7 +55,8 @@ constexpr int kTcStageBytes = 4 * kTcRegion;           // K lo, K hi, V lo, V hi
 constexpr int kTcRows = 32;                            // MMA N: query rows per KV head
 constexpr int kTcQHalf = kTcRows * 128;                // 4 KiB: 32 rows x 64 columns
 constexpr int kTcPBytes = 128 * 2 * kTcRows * 2;       // 16 KiB of bf16 P^T: high part | remainder
-constexpr int kTcThreads = 320;                        // producer, MMA, 2 x 4 softmax warps
+constexpr int kTcProducers = 3;                        // warps issuing TMA: 0, 10, 11
+constexpr int kTcThreads = 384;                        // producers, MMA, 2 x 4 softmax warps
 constexpr int kSoftmaxThreads = 256;
 constexpr int kWgThreads = 128;
 constexpr int kRowsWg = 16;                            // query rows per softmax warpgroup
@@ -227,8 +229,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int64_t x0 = share_start(N, cta, tw);
   const int64_t x1 = share_start(N, cta + 1, tw);
 
-  if (warp == 0) {
-    // =========================== TMA producer
+  if (warp == 0 || warp >= 10) {
+    // =========================== TMA producers: every producer warp walks the same tiles;
+    // warp 0 (pid 0) also writes the tile metadata, the expected byte count and the query
+    // block; the page boxes of a tile are spread over the producers (a warp pays ~86 cycles
+    // per box it issues, so one warp alone cannot keep a 64 KiB stage in flight).
+    const int pid = warp == 0 ? 0 : warp - 9;
     int t = 0;
     bool ok = true;
     const uint64_t policy = l2_policy_evict_first();
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) okw = wait_or_abort(&kv_empty[st], ph ^ 1u, abort_flag, a.err);
         if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
         const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
-        if (first_of_pair) {
+        if (first_of_pair && pid == 0) {
           if (lane == 0) okw = wait_or_abort(q_empty, static_cast<uint32_t>(q_uses & 1) ^ 1u, abort_flag, a.err);
           if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
           if (lane == 0) {
@@ -296,8 +302,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tma_load_4d(qbuf, &qmap, 0, h * a.G, 0, s, q_full);
             tma_load_4d(qbuf + kTcQHalf, &qmap, 64, h * a.G, 0, s, q_full);
           }
-          ++q_uses;
         }
+        if (first_of_pair) ++q_uses;
         const int src_lane = e - cbase + (lane & (kTcTilePages - 1));
         Entry en;
         en.lp = -1;
@@ -306,12 +312,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         en.phys = __shfl_sync(0xffffffffu, cache.phys, src_lane);
         const bool load = lane < n && en.phys >= 0;
         TileMeta& m = meta[st];
-        if (lane < kTcTilePages) {
+        if (pid == 0 && lane < kTcTilePages) {
           m.lo[lane] = load ? en.lo : 0;
           m.hi[lane] = load ? en.hi : 0;
         }
         const unsigned loadmask = __ballot_sync(0xffffffffu, load);
-        if (lane == 0) {
+        if (pid == 0 && lane == 0) {
           m.pair = pair;
           m.e0 = e;
           m.n = n;
@@ -321,9 +327,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m.start = pstart;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], __popc(loadmask) * 4u * kHalfBytes);
+        if (pid == 0 && lane == 0) mbar_arrive_expect_tx(&kv_full[st], __popc(loadmask) * 4u * kHalfBytes);
         __syncwarp();
-        if (load) {
+        if (load && (lane % kTcProducers) == pid) {
           uint8_t* dst = stages + static_cast<size_t>(st) * kTcStageBytes + lane * kHalfBytes;
           const int y = h * kPage;
           tma_load_3d(dst, &kmap, 0, y, en.phys, &kv_full[st], policy);
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         first_of_pair = false;
       }
     }
-    if (ok) {
+    if (ok && pid == 0) {
       // end marker for the MMA and softmax roles
       const int st = t % kTcStages;
       int okw = 1;
@@ -349,7 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     // Copies this warp may still have in flight (only after an abort).
-    if (lane == 0 && *abort_flag) {
+    if (pid == 0 && lane == 0 && *abort_flag) {
       for (int k = max(0, t - kTcStages); k < t; ++k)
         mbar_wait_bounded(&kv_full[k % kTcStages], static_cast<uint32_t>((k / kTcStages) & 1));
     }

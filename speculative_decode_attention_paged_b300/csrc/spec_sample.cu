@@ -283,35 +283,42 @@ __global__ void __launch_bounds__(256)
   if (tid == 0) chunk_sums[blockIdx.x] = t;
 }
 
-// One CTA per sequence: inverse CDF in token-id order.  The chunk sums give
-// the chunk holding u * Z; its tokens are split into contiguous runs, one per
-// thread, whose fp64 sums are prefix-summed in thread order; the thread whose
-// run spans the target walks it to the token.
-__global__ void __launch_bounds__(256)
+// One CTA per sequence: inverse CDF in token-id order.  The 32 chunk sums
+// (loaded in parallel) give the chunk holding u * Z; that chunk's residual
+// values are computed once into shared memory with coalesced loads, cut into
+// contiguous runs, one per thread, whose fp64 sums are prefix-summed in thread
+// order; the thread whose run spans the target walks it to the token.
+constexpr int kPickThreads = 256;
+constexpr int kPickMaxChunk = 8192;    // chunk values staged in shared memory (V <= 262,144)
+
+__global__ void __launch_bounds__(kPickThreads)
     pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
                 uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
                 const int32_t* __restrict__ accept, const double2* __restrict__ chunk_sums,
                 int32_t* __restrict__ out_tokens) {
-  __shared__ double s_excl[257];
+  __shared__ double2 s_cs[kSampleChunks];
+  __shared__ double s_excl[kPickThreads + 1];
+  __shared__ float s_r[kPickMaxChunk];
   __shared__ int s_chunk, s_use_p, s_pick, s_last;
   __shared__ double s_tgt;
   const int n = blockIdx.x;
   const int tid = threadIdx.x;
   const int a = __ldg(accept + n);
+  if (tid < kSampleChunks) s_cs[tid] = chunk_sums[static_cast<int64_t>(n) * kSampleChunks + tid];
+  __syncthreads();
   if (tid == 0) {
-    const double2* cs = chunk_sums + static_cast<int64_t>(n) * kSampleChunks;
     double zr = 0.0;
-    for (int c = 0; c < kSampleChunks; ++c) zr += cs[c].x;
+    for (int c = 0; c < kSampleChunks; ++c) zr += s_cs[c].x;
     const bool use_p = (a == k) || !(zr > 0.0);
     double Z = 0.0;
-    for (int c = 0; c < kSampleChunks; ++c) Z += use_p ? cs[c].y : cs[c].x;
+    for (int c = 0; c < kSampleChunks; ++c) Z += use_p ? s_cs[c].y : s_cs[c].x;
     const double target = static_cast<double>(philox_uniform(seed, offset, n, a, kStreamResample)) * Z;
     // First chunk whose inclusive prefix exceeds the target, else the last
     // chunk with positive mass.
     double run = 0.0, base = 0.0, last_base = 0.0;
     int pick = -1, last = 0;
     for (int c = 0; c < kSampleChunks; ++c) {
-      const double v = use_p ? cs[c].y : cs[c].x;
+      const double v = use_p ? s_cs[c].y : s_cs[c].x;
       if (v > 0.0) {
         last = c;
         last_base = run;
@@ -336,12 +343,19 @@ __global__ void __launch_bounds__(256)
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, s_use_p != 0);
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
-  const int E = (hi - lo + 255) / 256;
+  const int len = hi - lo;
+  const bool staged = len <= kPickMaxChunk;
+  if (staged) {
+    for (int v = tid; v < len; v += kPickThreads) s_r[v] = row.at(lo + v);
+    __syncthreads();
+  }
+  auto value = [&](int v) -> float { return staged ? s_r[v - lo] : row.at(v); };
+  const int E = (len + kPickThreads - 1) / kPickThreads;
   const int r0 = min(lo + tid * E, hi), r1 = min(r0 + E, hi);
   double part = 0.0;
   int my_last = -1;
   for (int v = r0; v < r1; ++v) {
-    const float r = row.at(v);
+    const float r = value(v);
     part += static_cast<double>(r);
     if (r > 0.f) my_last = v;
   }
@@ -351,12 +365,12 @@ __global__ void __launch_bounds__(256)
   if (tid == 0) {
     // Exclusive prefix in thread order, sequential so it is monotone.
     double run = 0.0;
-    for (int t = 0; t < 256; ++t) {
+    for (int t = 0; t < kPickThreads; ++t) {
       const double v = s_excl[t];
       s_excl[t] = run;
       run += v;
     }
-    s_excl[256] = __longlong_as_double(0x7ff0000000000000LL);   // +inf
+    s_excl[kPickThreads] = __longlong_as_double(0x7ff0000000000000LL);   // +inf
   }
   __syncthreads();
   const double tgt = s_tgt;
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(256)
     double run = s_excl[tid];
     int pick = -1;
     for (int v = r0; v < r1; ++v) {
-      const float r = row.at(v);
+      const float r = value(v);
       run += static_cast<double>(r);
       if (r > 0.f && run > tgt) {
         pick = v;
@@ -429,7 +443,7 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  pick_kernel<<<N, 256, 0, stream>>>(p, q, N, k, V, seed, offset, stats, accept, chunks, out_tokens);
+  pick_kernel<<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, accept, chunks, out_tokens);
   return cudaGetLastError();
 }
 
