@@ -50,6 +50,11 @@ using namespace attn;
 
 constexpr int kTcTilePages = 8;                        // 128 tokens: the MMA's M
 constexpr int kTcStages = 3;
+// Tile metadata ring, twice the stage ring: a stage's K half is reloaded as
+// soon as the score MMA has read it, while the output MMA and the softmax warps
+// of that tile still read its metadata; slot t % 6 is rewritten only for tile
+// t + 6, whose K waits for S(t + 3), which the issuer starts only after PV(t).
+constexpr int kMetaSlots = 2 * kTcStages;
 constexpr int kTcRegion = kTcTilePages * kHalfBytes;   // 16 KiB: one 64-column half of 8 pages
 constexpr int kTcStageBytes = 4 * kTcRegion;           // K lo, K hi, V lo, V hi halves
 constexpr int kTcRows = 32;                            // MMA N: query rows per KV head
@@ -85,8 +90,8 @@ __host__ __device__ inline TcSmem tc_smem_layout(int n_chunks) {
   s.stages = off;  off += static_cast<size_t>(kTcStages) * kTcStageBytes;
   s.q = off;       off += 2 * kTcQHalf;
   s.p = off;       off += kTcPBytes;
-  s.meta = off;    off += kTcStages * sizeof(TileMeta);
-  s.bars = off;    off += 16 * sizeof(uint64_t);
+  s.meta = off;    off += kMetaSlots * sizeof(TileMeta);
+  s.bars = off;    off += 32 * sizeof(uint64_t);
   s.red_max = off; off += 2 * 2 * 4 * 16 * sizeof(float);   // [group][buffer][quarter][row]
   s.red_sum = off; off += 2 * 4 * 16 * sizeof(float);       // [group][quarter][row]
   s.rowbuf = off;  off += 3 * 32 * sizeof(float);   // row LSE, row max, row 1/sum
@@ -153,15 +158,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* pbuf = smem + L.p;
   TileMeta* meta = reinterpret_cast<TileMeta*>(smem + L.meta);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* kv_full = bars;                 // [3]
-  uint64_t* kv_empty = bars + 3;            // [3]
-  uint64_t* q_full = bars + 6;
-  uint64_t* q_empty = bars + 7;
-  uint64_t* s_full = bars + 8;              // [2]
-  uint64_t* s_free = bars + 10;             // [2]
-  uint64_t* p_full = bars + 12;
-  uint64_t* o_done = bars + 13;
-  uint64_t* drain = bars + 14;
+  // K and V halves of a stage have their own full / empty barriers: K is free
+  // again as soon as the score MMA has read it, V once the output MMA has.
+  uint64_t* k_full = bars;                  // [3]
+  uint64_t* k_empty = bars + 3;             // [3]
+  uint64_t* v_full = bars + 6;              // [3]
+  uint64_t* v_empty = bars + 9;             // [3]
+  uint64_t* q_full = bars + 12;
+  uint64_t* q_empty = bars + 13;
+  uint64_t* s_full = bars + 14;             // [2]
+  uint64_t* s_free = bars + 16;             // [2]
+  uint64_t* p_full = bars + 18;
+  uint64_t* o_done = bars + 19;
+  uint64_t* drain = bars + 20;
+  // Softmax warps learn of tile t's metadata from meta_full[t % 6], not from
+  // k_full: K of a stage may be reloaded (k_full moving on) before they look.
+  uint64_t* meta_full = bars + 21;          // [kMetaSlots]
   float* red_max = reinterpret_cast<float*>(smem + L.red_max);
   float* red_sum = reinterpret_cast<float*>(smem + L.red_sum);
   float* row_lse = reinterpret_cast<float*>(smem + L.rowbuf);    // [32]
@@ -179,8 +191,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -191,6 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(p_full, 8);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    for (int s = 0; s < kMetaSlots; ++s) mbar_init(&meta_full[s], 1);
     *abort_flag = 0;
     *last_flag = 0;
   }
@@ -291,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int st = t % kTcStages;
         const uint32_t ph = static_cast<uint32_t>((t / kTcStages) & 1);
         int okw = 1;
-        if (lane == 0) okw = wait_or_abort(&kv_empty[st], ph ^ 1u, abort_flag, a.err);
+        if (lane == 0) okw = wait_or_abort(&k_empty[st], ph ^ 1u, abort_flag, a.err);
         if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
         const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
         if (first_of_pair && pid == 0) {
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         en.hi = __shfl_sync(0xffffffffu, cache.hi, src_lane);
         en.phys = __shfl_sync(0xffffffffu, cache.phys, src_lane);
         const bool load = lane < n && en.phys >= 0;
-        TileMeta& m = meta[st];
+        TileMeta& m = meta[t % kMetaSlots];
         if (pid == 0 && lane < kTcTilePages) {
           m.lo[lane] = load ? en.lo : 0;
           m.hi[lane] = load ? en.hi : 0;
@@ -327,15 +342,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m.start = pstart;
         }
         __syncwarp();
-        if (pid == 0 && lane == 0) mbar_arrive_expect_tx(&kv_full[st], __popc(loadmask) * 4u * kHalfBytes);
+        if (pid == 0 && lane == 0) {
+          mbar_arrive(&meta_full[t % kMetaSlots]);
+          mbar_arrive_expect_tx(&k_full[st], __popc(loadmask) * 2u * kHalfBytes);
+        }
         __syncwarp();
-        if (load && (lane % kTcProducers) == pid) {
-          uint8_t* dst = stages + static_cast<size_t>(st) * kTcStageBytes + lane * kHalfBytes;
-          const int y = h * kPage;
-          tma_load_3d(dst, &kmap, 0, y, en.phys, &kv_full[st], policy);
-          tma_load_3d(dst + kTcRegion, &kmap, 64, y, en.phys, &kv_full[st], policy);
-          tma_load_3d(dst + 2 * kTcRegion, &vmap, 0, y, en.phys, &kv_full[st], policy);
-          tma_load_3d(dst + 3 * kTcRegion, &vmap, 64, y, en.phys, &kv_full[st], policy);
+        const bool mine = load && (lane % kTcProducers) == pid;
+        uint8_t* dst = stages + static_cast<size_t>(st) * kTcStageBytes + lane * kHalfBytes;
+        const int y = h * kPage;
+        if (mine) {
+          tma_load_3d(dst, &kmap, 0, y, en.phys, &k_full[st], policy);
+          tma_load_3d(dst + kTcRegion, &kmap, 64, y, en.phys, &k_full[st], policy);
+        }
+        // V of this tile once the output MMA of the stage's previous tile is done
+        if (lane == 0) okw = wait_or_abort(&v_empty[st], ph ^ 1u, abort_flag, a.err);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
+        if (pid == 0 && lane == 0) mbar_arrive_expect_tx(&v_full[st], __popc(loadmask) * 2u * kHalfBytes);
+        __syncwarp();
+        if (mine) {
+          tma_load_3d(dst + 2 * kTcRegion, &vmap, 0, y, en.phys, &v_full[st], policy);
+          tma_load_3d(dst + 3 * kTcRegion, &vmap, 64, y, en.phys, &v_full[st], policy);
         }
         x += n;
         e += n;
@@ -347,17 +373,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // end marker for the MMA and softmax roles
       const int st = t % kTcStages;
       int okw = 1;
-      if (lane == 0) okw = wait_or_abort(&kv_empty[st], static_cast<uint32_t>((t / kTcStages) & 1) ^ 1u,
+      if (lane == 0) okw = wait_or_abort(&k_empty[st], static_cast<uint32_t>((t / kTcStages) & 1) ^ 1u,
                                          abort_flag, a.err);
       if (__shfl_sync(0xffffffffu, okw, 0) && lane == 0) {
-        meta[st].flags = kTileEnd;
-        mbar_arrive(&kv_full[st]);
+        meta[t % kMetaSlots].flags = kTileEnd;
+        mbar_arrive(&meta_full[t % kMetaSlots]);
+        mbar_arrive(&k_full[st]);
       }
     }
     // Copies this warp may still have in flight (only after an abort).
     if (pid == 0 && lane == 0 && *abort_flag) {
-      for (int k = max(0, t - kTcStages); k < t; ++k)
-        mbar_wait_bounded(&kv_full[k % kTcStages], static_cast<uint32_t>((k / kTcStages) & 1));
+      for (int k = max(0, t - kTcStages); k < t; ++k) {
+        mbar_wait_bounded(&k_full[k % kTcStages], static_cast<uint32_t>((k / kTcStages) & 1));
+        mbar_wait_bounded(&v_full[k % kTcStages], static_cast<uint32_t>((k / kTcStages) & 1));
+      }
     }
   } else if (warp == 1) {
     // =========================== MMA issuer (one thread)
@@ -385,38 +414,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           umma_bf16(tmem + kColS + 32u * b, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[b]);
+        umma_commit(&k_empty[st]);            // K of this stage may be reloaded
         if (flags & kTileLast) umma_commit(q_empty);
         return true;
       };
-      int t = 0;
-      int flags = kTileEnd;
-      if (wait_or_abort(&kv_full[0], 0, abort_flag, a.err)) {
-        flags = meta[0].flags;
-        if (!(flags & kTileEnd)) ok = issue_s(0, flags);
+      auto ph_of = [](int x) { return static_cast<uint32_t>((x / kTcStages) & 1); };
+      // S(t) is issued as soon as tile t's K lands; PV(t) as soon as its P is
+      // written: the issuer polls both, so a late K never holds back a PV.
+      int t = 0, s_next = 0;
+      bool end_seen = false;
+      if (wait_or_abort(&k_full[0], 0, abort_flag, a.err)) {
+        const int f = meta[0].flags;
+        if (f & kTileEnd) end_seen = true;
+        else if ((ok = issue_s(0, f))) s_next = 1;
       } else {
         ok = false;
       }
-      while (ok && !(flags & kTileEnd)) {
-        const int nx = t + 1;
-        const int st1 = nx % kTcStages;
-        if (!wait_or_abort(&kv_full[st1], static_cast<uint32_t>((nx / kTcStages) & 1), abort_flag, a.err)) {
-          ok = false;
-          break;
+      while (ok && s_next > t) {
+        for (uint32_t spin = 0;; ++spin) {
+          if (!end_seen && s_next == t + 1 && mbar_test_wait(&k_full[s_next % kTcStages], ph_of(s_next))) {
+            const int f = meta[s_next % kMetaSlots].flags;
+            if (f & kTileEnd) {
+              end_seen = true;
+            } else {
+              if (!issue_s(s_next, f)) { ok = false; break; }
+              ++s_next;
+            }
+          }
+          if (mbar_test_wait(p_full, static_cast<uint32_t>(t & 1))) break;
+          if (*abort_flag) { ok = false; break; }
+          if (spin >= 16u * kMaxSpin) {
+            *abort_flag = 1;
+            report_error(a.err, S3R_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
         }
-        const int flags1 = meta[st1].flags;
-        if (!(flags1 & kTileEnd) && !issue_s(nx, flags1)) {
-          ok = false;
-          break;
-        }
+        if (!ok) break;
         // O^T += V^T P^T for tile t
-        if (!wait_or_abort(p_full, static_cast<uint32_t>(t & 1), abort_flag, a.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
         const int st = t % kTcStages;
-        const int n = meta[st].n;
-        const bool first = (flags & kTileFirst) != 0;
+        if (!wait_or_abort(&v_full[st], ph_of(t), abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after_sync();
+        const int n = meta[t % kMetaSlots].n;
+        const bool first = (meta[t % kMetaSlots].flags & kTileFirst) != 0;
         const uint64_t vd0 = umma_smem_desc(smem_u32(stages + static_cast<size_t>(st) * kTcStageBytes) +
                                                 2 * kTcRegion,
                                             kTcRegion, 1024, kUmmaLayoutSw128);
@@ -427,9 +467,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     pd0 + static_cast<uint64_t>((p * 2048) >> 4), idesc_o, (first && p == 0) ? 0u : 1u);
         }
         umma_commit(o_done);
-        umma_commit(&kv_empty[st]);
-        t = nx;
-        flags = flags1;
+        umma_commit(&v_empty[st]);
+        ++t;
+        if (s_next == t && !end_seen) {      // S(t) still waits for its K
+          if (!wait_or_abort(&k_full[t % kTcStages], ph_of(t), abort_flag, a.err)) { ok = false; break; }
+          const int f = meta[t % kMetaSlots].flags;
+          if (f & kTileEnd) end_seen = true;
+          else if ((ok = issue_s(t, f))) ++s_next;
+        }
       }
       if (!ok) *abort_flag = 1;
       // no MMA may be in flight when the TMEM is freed
@@ -456,10 +501,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     int seg_index = 0;
     for (int t = 0;; ++t) {
-      const int st = t % kTcStages;
       const int b = t & 1;
-      bool ok = wait_or_abort(&kv_full[st], static_cast<uint32_t>((t / kTcStages) & 1), abort_flag, a.err);
-      const TileMeta& m = meta[st];
+      bool ok = wait_or_abort(&meta_full[t % kMetaSlots], static_cast<uint32_t>((t / kMetaSlots) & 1),
+                              abort_flag, a.err);
+      const TileMeta& m = meta[t % kMetaSlots];
       const int flags = ok ? m.flags : kTileEnd;
       if (ok && !(flags & kTileEnd))
         ok = wait_or_abort(&s_full[b], static_cast<uint32_t>((t >> 1) & 1), abort_flag, a.err);
