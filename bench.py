@@ -272,6 +272,12 @@ def dist_setup(n_gpus):
     return world, rank, local
 
 
+def aggregate_gbs(step_bytes, ms_per_step, world):
+    """Whole-job throughput of `world` replicas each moving step_bytes per
+    step, timed by the slowest rank (ms_per_step = max over ranks)."""
+    return world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -446,7 +452,7 @@ def run_s3r(args, world, rank, local):
     pm = {key: statistics.mean(v) for key, v in ph.items()}
 
     ms_per_step = total_ms_max / K
-    value = world * w.step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = aggregate_gbs(w.step_bytes, ms_per_step, world)
     b = w.bytes
     dense_avg_bytes = sum(b["dense"]) / k
     dense_launch = statistics.mean(dense_launch_ms)
