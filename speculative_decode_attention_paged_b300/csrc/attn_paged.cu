@@ -244,25 +244,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Slot of segment j of a pair cut by warp shares: the pair's pages start at
   // global index X and span shares gwa..; with N >= tw every share holds a
-  // page, otherwise every non-empty share holds exactly one page.
-  auto segment_slot = [&](int64_t X, int gwa, int j) -> int {
-    if (N >= tw) return (gwa + j) * 2 + ((j == 0 && share_start(N, gwa, tw) < X) ? 1 : 0);
+  // page, otherwise every non-empty share holds exactly one page.  a_off: the
+  // first share started before the pair (its partial is that warp's second).
+  auto segment_slot = [&](int64_t X, int gwa, bool a_off, int j) -> int {
+    if (N >= tw) return (gwa + j) * 2 + ((j == 0 && a_off) ? 1 : 0);
     return share_of(N, X + j, tw) * 2;
   };
 
-  // Merge the partials of the current (cut) pair: lane r < R folds row r's
-  // (m, l) over the segments, then every lane merges 4 of the 128 columns.
+  // Merge the partials of the current (cut) pair.  Pass 1: lane r < R folds
+  // row r's (m, l) over the segments, eight loads in flight at a time.  Pass 2:
+  // every lane merges 4 of the 128 columns of each row, again with the loads
+  // of eight segments issued together.
   auto merge_pair = [&](int nseg, int gwa) {
+    constexpr int kBatch = 8;
+    const bool a_off = N >= tw && share_start(N, gwa, tw) < cur_start;
     float M = kNegInf, Ls = 0.f;
     if (lane < a.R) {
-      for (int j = 0; j < nseg; ++j) {
-        const int slot = segment_slot(cur_start, gwa, j);
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-            a.part_ml + (static_cast<int64_t>(slot) * a.R + lane) * 2));
-        if (ml.y > 0.f) {
-          const float mn = fmaxf(M, ml.x);
-          Ls = Ls * fast_exp2(M - mn) + ml.y * fast_exp2(ml.x - mn);
-          M = mn;
+      for (int j0 = 0; j0 < nseg; j0 += kBatch) {
+        float2 ml[kBatch];
+#pragma unroll
+        for (int jj = 0; jj < kBatch; ++jj) {
+          const int j = j0 + jj;
+          ml[jj] = j < nseg ? __ldcg(reinterpret_cast<const float2*>(
+                                  a.part_ml + (static_cast<int64_t>(segment_slot(cur_start, gwa, a_off, j)) * a.R +
+                                               lane) * 2))
+                            : make_float2(kNegInf, 0.f);
+        }
+#pragma unroll
+        for (int jj = 0; jj < kBatch; ++jj) {
+          if (ml[jj].y > 0.f) {
+            const float mn = fmaxf(M, ml[jj].x);
+            Ls = Ls * fast_exp2(M - mn) + ml[jj].y * fast_exp2(ml[jj].x - mn);
+            M = mn;
+          }
         }
       }
       if (MASS) my_lse[lane] = Ls > 0.f ? M + fast_log2(Ls) : kNegInf;
@@ -272,16 +286,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float Mr = __shfl_sync(0xffffffffu, M, r);
       const float ir = __shfl_sync(0xffffffffu, inv, r);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < nseg; ++j) {
-        const int slot = segment_slot(cur_start, gwa, j);
-        const int64_t row = static_cast<int64_t>(slot) * a.R + r;
-        const float mr = __ldcg(a.part_ml + row * 2);
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * kHeadDim) + lane);
-        const float w = mr == kNegInf ? 0.f : fast_exp2(mr - Mr) * ir;
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
+      for (int j0 = 0; j0 < nseg; j0 += kBatch) {
+        float mr[kBatch];
+        float4 o[kBatch];
+#pragma unroll
+        for (int jj = 0; jj < kBatch; ++jj) {
+          const int j = j0 + jj;
+          if (j < nseg) {
+            const int64_t row = static_cast<int64_t>(segment_slot(cur_start, gwa, a_off, j)) * a.R + r;
+            mr[jj] = __ldcg(a.part_ml + row * 2);
+            o[jj] = __ldcg(reinterpret_cast<const float4*>(a.part_o + row * kHeadDim) + lane);
+          } else {
+            mr[jj] = kNegInf;
+            o[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < kBatch; ++jj) {
+          const float w = mr[jj] == kNegInf ? 0.f : fast_exp2(mr[jj] - Mr) * ir;
+          acc.x += w * o[jj].x;
+          acc.y += w * o[jj].y;
+          acc.z += w * o[jj].z;
+          acc.w += w * o[jj].w;
+        }
       }
       reinterpret_cast<float4*>(a.out + q_row_offset(r))[lane] = acc;
     }

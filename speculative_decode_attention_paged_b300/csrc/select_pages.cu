@@ -59,12 +59,12 @@ __global__ void __launch_bounds__(kSelWarps * 32)
   }
   {
     int pg = lane;
-    for (; pg + 7 * 32 < P; pg += 8 * 32) {
-      float v[8];
+    for (; pg + 15 * 32 < P; pg += 16 * 32) {   // 16 loads in flight per lane
+      float v[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __ldg(grow + pg + j * 32);
+      for (int j = 0; j < 16; ++j) v[j] = __ldg(grow + pg + j * 32);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) row[pg + j * 32] = v[j];
+      for (int j = 0; j < 16; ++j) row[pg + j * 32] = v[j];
     }
     for (; pg < P; pg += 32) row[pg] = __ldg(grow + pg);
     __syncwarp();

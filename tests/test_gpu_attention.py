@@ -37,7 +37,7 @@ def _check_mass(mass_gpu, mass_ref, rows):
 RAGGED = [1, 2, 15, 16, 17, 31, 32, 33, 47, 100, 255, 256, 257, 1000, 1023, 2049, 3001]
 
 
-@pytest.mark.parametrize("q_heads,kv_heads", [(16, 8), (32, 8), (8, 8), (4, 1), (16, 2)])
+@pytest.mark.parametrize("q_heads,kv_heads", [(16, 8), (32, 8), (8, 8), (4, 1), (16, 2), (24, 1), (32, 1)])
 def test_dense_decode_ragged(q_heads, kv_heads):
     lens = RAGGED + [5, 600, 64]
     kv = make_paged_kv(len(lens), q_heads, kv_heads, 4, seed=101, device=DEV, hist_lens=lens)
@@ -129,7 +129,7 @@ def _random_selection(kv, rng, b_max, count_lo=0):
     return sel, cnt
 
 
-@pytest.mark.parametrize("q_heads,kv_heads", [(16, 8), (32, 8), (4, 1)])
+@pytest.mark.parametrize("q_heads,kv_heads", [(16, 8), (32, 8), (4, 1), (32, 1)])
 def test_sparse_draft_random_selections(q_heads, kv_heads):
     lens = RAGGED
     kv = make_paged_kv(len(lens), q_heads, kv_heads, 4, seed=106, device=DEV, hist_lens=lens)
