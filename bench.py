@@ -698,8 +698,19 @@ def run_sampler(args):
         del inp
         torch.cuda.empty_cache()
     vals = [r["gbs"] for r in res.values()]
+    # draft-token sampling: one token per sequence from softmax(q) of one draft step
+    g = torch.Generator(device=dev)
+    g.manual_seed(sc.seed + 7)
+    logits = torch.randn((N, sc.vocab), generator=g, device=dev) * sc.p_sigma
+    dws = s3r.Workspace(s3r.s3r_sample_draft_workspace_size(N), device=dev)
+    dtok = torch.empty((N,), dtype=torch.int32, device=dev)
+    t = _timed(lambda: s3r.s3r_sample_draft_tokens(logits, sc.philox_seed, 0, 0, dtok, dws), args.steps, args.warmup)
+    dws.check()
+    dbytes = N * sc.vocab * 4 + N * 4
+    draft = {"ms": t, "gb": dbytes / 1e9, "gbs": dbytes / (t * 1e-3) / 1e9, "tokens_per_s": N / (t * 1e-3)}
     return {"workload": f"spec sample: {N} seqs x k={sc.k} x V={sc.vocab} fp32, p~N(0,3^2), q=p+N(0,s^2)",
-            "metric": METRIC, "value": float(np.mean(vals)), "unit": UNIT, "sigma": res}
+            "metric": METRIC, "value": float(np.mean(vals)), "unit": UNIT, "sigma": res,
+            "draft_token_sampling": draft}
 
 
 def run_layers(args):

@@ -234,6 +234,26 @@ S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
                            uint64_t seed, uint64_t offset, int32_t* out_tokens,
                            int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
 
+/* Workspace bytes for s3r_sample_draft_tokens with n sequences (host). */
+S3R_API s3r_status s3r_sample_draft_workspace_size(int32_t n, size_t* bytes);
+
+/*
+ * Draft-token sampling: the drafter proposes each token by sampling from its
+ * own distribution q (wispaper.ai, "S3R drafts sparsely and verifies densely";
+ * rebasdaily.com, "草稿可以稀疏，交卷必须完整"), here at draft step
+ * `draft_pos` of every sequence.
+ *
+ *   logits  fp32 [n][vocab], the drafter's logits at this step
+ *   tokens  int32 [n] out
+ * token[s] is the inverse CDF, in token-id order, of softmax(logits[s])
+ * (temperature 1) at the Philox4x32-10 uniform of counter
+ * (s, draft_pos, 2, offset) and key seed (stream 2 = DRAFT), with the same
+ * uniform and inverse-CDF conventions as s3r_spec_sample.  offset < 2^32.
+ */
+S3R_API s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, uint64_t seed,
+                                   uint64_t offset, int32_t draft_pos, int32_t* tokens, void* ws,
+                                   size_t ws_bytes, void* stream);
+
 /* Bytes of library-owned device scratch behind s3r_spec_sample_noalloc, held
  * once by every GPU that loads the library until the process exits. */
 #define S3R_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)

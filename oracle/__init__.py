@@ -33,6 +33,7 @@ from .attention import (
 from .selection import select_draft_pages, selection_budget
 from .philox import philox4x32_10, philox_uniform, STREAM_ACCEPT, STREAM_RESAMPLE, STREAM_DRAFT
 from .spec_sample import spec_sample, residual_row
+from .draft_sample import sample_draft_tokens
 
 __all__ = [
     "PAGE_SIZE",
@@ -49,4 +50,5 @@ __all__ = [
     "STREAM_DRAFT",
     "spec_sample",
     "residual_row",
+    "sample_draft_tokens",
 ]

@@ -30,6 +30,8 @@ __all__ = [
     "s3r_select_draft_pages",
     "s3r_spec_sample",
     "s3r_spec_sample_noalloc",
+    "s3r_sample_draft_workspace_size",
+    "s3r_sample_draft_tokens",
     "DEVERR_BAD_PAGE",
     "DEVERR_BAD_LENGTH",
     "DEVERR_BAD_TOKEN",
@@ -100,6 +102,9 @@ _SIG = {
                                        _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
                                                _P, _P, _P, _P]),
+    "s3r_sample_draft_workspace_size": (ctypes.c_int, [_I32, ctypes.POINTER(ctypes.c_size_t)]),
+    "s3r_sample_draft_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64, _I32, _P, _P,
+                                               ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -316,3 +321,19 @@ def s3r_spec_sample_noalloc(p_logits, q_logits, draft_tokens, seed, offset, out_
           _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted),
           _ptr(device_error), _stream(stream))
     return out_tokens, n_accepted
+
+
+def s3r_sample_draft_workspace_size(n):
+    out = ctypes.c_size_t(0)
+    _call("s3r_sample_draft_workspace_size", _I32(n), ctypes.byref(out))
+    return out.value
+
+
+def s3r_sample_draft_tokens(logits, seed, offset, draft_pos, tokens, ws: Workspace, stream=None):
+    """One draft token per sequence from softmax(logits) [n][vocab] (fp32)."""
+    _need(logits, torch.float32, "logits")
+    _need(tokens, torch.int32, "tokens")
+    n, V = logits.shape
+    _call("s3r_sample_draft_tokens", _ptr(logits), _I32(n), _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset),
+          _I32(draft_pos), _ptr(tokens), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return tokens

@@ -24,6 +24,7 @@ using namespace s3r;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSpecK = 64;
+constexpr uint32_t kStreamDraftU = 2;   // Philox stream of draft-token sampling
 // Longest mass row the selection kernel stages in shared memory (pages).
 constexpr int kMaxSelectPages = 49152;
 
@@ -337,6 +338,31 @@ s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
   return to_status(launch_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
                                       static_cast<uint32_t>(offset), ws, out_tokens, n_accepted,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, uint64_t seed,
+                                   uint64_t offset, int32_t draft_pos, int32_t* tokens, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  if (n < 0 || vocab <= 0 || draft_pos < 0) return S3R_ERR_INVALID_ARG;
+  if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n) * vocab > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(n) * kSampleChunks > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
+  size_t need = 0;
+  s3r_sample_draft_workspace_size(n, &need);
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < need) return S3R_ERR_WORKSPACE;
+  if (n == 0) return S3R_OK;
+  if (logits == nullptr || tokens == nullptr) return S3R_ERR_INVALID_ARG;
+  const SpecWorkspaceLayout L = spec_workspace_layout(n, 0);
+  int32_t* count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.accept_off);
+  return to_status(launch_spec_sample(logits, nullptr, nullptr, n, 0, vocab, seed, static_cast<uint32_t>(offset),
+                                      ws, tokens, count, static_cast<cudaStream_t>(stream), kStreamDraftU,
+                                      draft_pos));
+}
+
+s3r_status s3r_sample_draft_workspace_size(int32_t n, size_t* bytes) {
+  if (bytes == nullptr || n < 0) return S3R_ERR_INVALID_ARG;
+  *bytes = spec_workspace_layout(n, 0).total;
+  return S3R_OK;
 }
 
 }  // extern "C"

@@ -293,7 +293,8 @@ constexpr int kPickMaxChunk = 8192;    // chunk values staged in shared memory (
 
 __global__ void __launch_bounds__(kPickThreads)
     pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
-                uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
+                uint64_t seed, uint32_t offset, uint32_t u_stream, int u_pos,
+                const float2* __restrict__ stats,
                 const int32_t* __restrict__ accept, const double2* __restrict__ chunk_sums,
                 int32_t* __restrict__ out_tokens) {
   __shared__ double2 s_cs[kSampleChunks];
@@ -312,7 +313,10 @@ __global__ void __launch_bounds__(kPickThreads)
     const bool use_p = (a == k) || !(zr > 0.0);
     double Z = 0.0;
     for (int c = 0; c < kSampleChunks; ++c) Z += use_p ? s_cs[c].y : s_cs[c].x;
-    const double target = static_cast<double>(philox_uniform(seed, offset, n, a, kStreamResample)) * Z;
+    // the uniform of counter (n, position, stream, offset): position a on the
+    // RESAMPLE stream for verification, the draft step on the DRAFT stream
+    const double target =
+        static_cast<double>(philox_uniform(seed, offset, n, u_pos >= 0 ? u_pos : a, u_stream)) * Z;
     // First chunk whose inclusive prefix exceeds the target, else the last
     // chunk with positive mass.
     double run = 0.0, base = 0.0, last_base = 0.0;
@@ -411,7 +415,8 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
 
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                int V, uint64_t seed, uint32_t offset, void* ws,
-                               int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream) {
+                               int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
+                               uint32_t u_stream, int u_pos) {
   if (N == 0) return cudaSuccess;
   const SpecWorkspaceLayout L = spec_workspace_layout(N, k);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -443,7 +448,8 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  pick_kernel<<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, accept, chunks, out_tokens);
+  pick_kernel<<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, u_stream, u_pos, stats, accept,
+                                              chunks, out_tokens);
   return cudaGetLastError();
 }
 

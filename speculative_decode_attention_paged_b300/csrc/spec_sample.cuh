@@ -22,9 +22,13 @@ struct SpecWorkspaceLayout {
 SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k);
 
 // Enqueue the four sampler kernels.  `ws` is the caller's workspace laid out
-// by spec_workspace_layout(N, k).
+// by spec_workspace_layout(N, k).  The final inverse CDF draws the Philox
+// uniform of counter (n, u_pos, u_stream, offset); u_pos < 0 means the
+// sequence's accepted count (verification: stream RESAMPLE).  With k = 0 and
+// no draft rows this samples one token from softmax(p) per sequence.
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                int V, uint64_t seed, uint32_t offset, void* ws,
-                               int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream);
+                               int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
+                               uint32_t u_stream = 1, int u_pos = -1);
 
 }  // namespace s3r

@@ -11,10 +11,12 @@ import textwrap
 import pytest
 
 import oracle.attention as oatt
+import oracle.draft_sample as odraft
 import oracle.philox as ophil
 import oracle.selection as osel
 import oracle.spec_sample  # noqa: F401  (the package re-exports a function of the same name)
 import test_oracle_attention as pins_att
+import test_oracle_draft_sample as pins_draft
 import test_oracle_philox as pins_phil
 import test_oracle_select as pins_sel
 import test_oracle_spec_sample as pins_spec
@@ -113,3 +115,9 @@ def test_bonus_from_the_draft_row_is_caught(monkeypatch):
     mutant = _mutant(ospec, "spec_sample", "row[~rej] = p[pn[~rej], k]", "row[~rej] = q[qn[~rej], k - 1]")
     monkeypatch.setattr(pins_spec, "spec_sample", mutant)
     _fails(pins_spec.test_output_distribution_equals_target)
+
+
+def test_draft_sampler_on_the_wrong_stream_is_caught(monkeypatch):
+    mutant = _mutant(odraft, "sample_draft_tokens", "int(draft_pos), STREAM_DRAFT)", "int(draft_pos), 1)")
+    monkeypatch.setattr(pins_draft, "sample_draft_tokens", mutant)
+    _fails(pins_draft.test_uniform_logits_give_floor_u_times_v)
