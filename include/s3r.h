@@ -273,7 +273,7 @@ S3R_API s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32
  *                 call's device error bits (the S3R_DEVERR_* values)
  * Returns S3R_ERR_UNSUPPORTED, before enqueuing anything, when
  * s3r_spec_sample_workspace_size(n, k) exceeds S3R_NOALLOC_SCRATCH_BYTES
- * (for example n = 2048 with k = 8 needs 1,335,552 bytes and fits).
+ * (for example n = 2048 with k = 8 needs 1,859,840 bytes and fits).
  * The first call on each device looks up the array's device address (a
  * one-time set-up per device, with that device current): make that first
  * call before any stream capture.  Every call on a device shares the one

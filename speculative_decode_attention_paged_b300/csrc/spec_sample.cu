@@ -7,20 +7,25 @@
 // from the residual distribution (rit.work, "Как разреженный черновик
 // сохраняет ответы плотной модели"; rebasdaily.com, "草稿可以稀疏，交卷必须完整").
 //
-// Four kernels, all parallel over rows or chunks of rows:
+// Kernels, all parallel over rows or chunks of rows.  Each row is cut into 32
+// contiguous chunks.
 //   row_stats   one CTA per logit row (k+1 target rows and k draft rows per
-//               sequence): the row max m and z = sum_v 2^((x_v - m) log2 e),
-//               one streaming pass with 16-byte loads;
+//               sequence), one warp per chunk: the row max m and
+//               z = sum_v 2^((x_v - m) log2 e) in one streaming pass with
+//               16-byte loads; the bonus row p_k also keeps its 32 chunk
+//               (max, sum) pairs, which are its chunk masses;
 //   accept      one warp per sequence: the k ratio tests p_i(x_i)/q_i(x_i)
 //               against Philox uniforms (fp64 ratio from fp32 row stats);
 //               a = the first rejected position (k if none);
-//   chunk_sum   one CTA per (sequence, chunk of the row): fp64 sums over the
-//               chunk of the residual max(0, p_a - q_a) (or of p_k for the
-//               bonus token) and of p_a (the fallback when the residual
-//               vanishes);
-//   pick        one CTA per sequence: the chunk sums locate the chunk holding
-//               u * Z; that chunk alone is scanned in token-id order (fp64
-//               prefix over contiguous per-thread runs) to find the token.
+//   chunk_sum   one CTA per (sequence, chunk) of a sequence that rejected:
+//               fp64 sums over the chunk of the residual max(0, p_a - q_a)
+//               and of p_a (the fallback when the residual vanishes);
+//   pick        one CTA per sequence: the chunk masses locate the chunk
+//               holding u * Z; that chunk alone is scanned in token-id order
+//               (fp32 sums over contiguous per-thread runs, fp64 prefix across
+//               runs) to find the token.
+// With k = 0 there is nothing to test and the row is its own bonus row:
+// bonus_sample does row_stats and pick for one sequence in one CTA.
 
 #include <cfloat>
 
@@ -49,25 +54,26 @@ __device__ __forceinline__ void merge_stats(float& m, float& z, float m2, float 
   m = mn;
 }
 
+// Contiguous chunk `c` of a row of V tokens: [lo, hi).  The chunk length is a
+// multiple of 4 so float4 loads stay aligned when V is.
+__device__ __forceinline__ int chunk_len(int V) {
+  return ((V + kSampleChunks - 1) / kSampleChunks + 3) & ~3;
+}
+
+// One warp streams x[lo, hi) once: the online maximum m and
+// z = sum 2^((x - m) log2 e), merged across the warp (lane 0 holds the result).
 template <bool VEC>
-__global__ void __launch_bounds__(kStatThreads)
-    row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
-                     float2* __restrict__ stats) {
-  const int row = blockIdx.x;
-  const int np = N * (k + 1);
-  const float* x = row < np ? p + static_cast<int64_t>(row) * V
-                            : q + static_cast<int64_t>(row - np) * V;
-  const int tid = threadIdx.x;
+__device__ __forceinline__ float2 warp_chunk_stats(const float* __restrict__ x, int lo, int hi, int lane) {
   const float neg_inf = -__builtin_huge_valf();
   float m = neg_inf, z = 0.f;
   if (VEC) {
-    const float4* x4 = reinterpret_cast<const float4*>(x);
-    const int n4 = V >> 2;
-    for (int base = 0; base < n4; base += 4 * kStatThreads) {
+    const float4* x4 = reinterpret_cast<const float4*>(x + lo);
+    const int n4 = (hi - lo) >> 2;
+    for (int base = 0; base < n4; base += 4 * 32) {
       float4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int idx = base + j * kStatThreads + tid;
+        const int idx = base + j * 32 + lane;
         v[j] = idx < n4 ? __ldcs(x4 + idx) : make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
       }
       float bm = neg_inf;
@@ -87,12 +93,12 @@ __global__ void __launch_bounds__(kStatThreads)
       z += bs;
     }
   } else {
-    for (int base = 0; base < V; base += 4 * kStatThreads) {
+    for (int base = lo; base < hi; base += 4 * 32) {
       float v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int idx = base + j * kStatThreads + tid;
-        v[j] = idx < V ? __ldcs(x + idx) : neg_inf;
+        const int idx = base + j * 32 + lane;
+        v[j] = idx < hi ? __ldcs(x + idx) : neg_inf;
       }
       const float bm = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
       if (bm > m) {
@@ -104,38 +110,85 @@ __global__ void __launch_bounds__(kStatThreads)
       z += (scaled_exp(v[0], ml) + scaled_exp(v[1], ml)) + (scaled_exp(v[2], ml) + scaled_exp(v[3], ml));
     }
   }
-  // Block reduction of (m, z).
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
     const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
     merge_stats(m, z, m2, z2);
   }
-  __shared__ float sm[kStatThreads / 32], sz[kStatThreads / 32];
-  if ((tid & 31) == 0) {
-    sm[tid >> 5] = m;
-    sz[tid >> 5] = z;
+  return make_float2(m, z);
+}
+
+// The whole CTA streams row x once; warp w takes chunks w, w + 8, ...; the
+// per-chunk (max, sum) land in s_c[kSampleChunks].  Ends with a barrier.
+template <bool VEC>
+__device__ __forceinline__ void block_chunk_stats(const float* __restrict__ x, int V, float2* s_c) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int CL = chunk_len(V);
+  for (int c = warp; c < kSampleChunks; c += kStatThreads / 32) {
+    const int lo = min(c * CL, V), hi = min(lo + CL, V);
+    const float2 s = warp_chunk_stats<VEC>(x, lo, hi, lane);
+    if (lane == 0) s_c[c] = s;
   }
   __syncthreads();
-  if (tid == 0) {
-    float M = sm[0], Z = sz[0];
-    for (int w = 1; w < kStatThreads / 32; ++w) merge_stats(M, Z, sm[w], sz[w]);
-    stats[row] = make_float2(M, Z);
+}
+
+// Warp-wide: lane c holds chunk c's (max, sum); the row's (max, sum) in lane 0.
+__device__ __forceinline__ float2 merge_chunk_stats(float2 s) {
+  float m = s.x, z = s.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float z2 = __shfl_xor_sync(0xffffffffu, z, o);
+    merge_stats(m, z, m2, z2);
+  }
+  return make_float2(m, z);
+}
+
+// Probability mass of a chunk from its statistics and the row's:
+// z_c 2^((m_c - m) log2 e) / z, in fp64; 0 for an empty chunk (and for the
+// undefined all -inf row).
+__device__ __forceinline__ double chunk_mass(float2 c, float2 row) {
+  const double v = static_cast<double>(c.y) *
+                   exp2((static_cast<double>(c.x) - static_cast<double>(row.x)) * kLog2eD) /
+                   static_cast<double>(row.y);
+  return v > 0.0 ? v : 0.0;
+}
+
+// One CTA per logit row (k+1 target rows, then k draft rows per sequence):
+// the row's (max, sum) and, for the bonus row p_k, its 32 chunk statistics,
+// which give the bonus row's chunk masses without a second pass.
+template <bool VEC>
+__global__ void __launch_bounds__(kStatThreads)
+    row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
+                     float2* __restrict__ stats, float2* __restrict__ bonus_chunks) {
+  const int row = blockIdx.x;
+  const int np = N * (k + 1);
+  const float* x = row < np ? p + static_cast<int64_t>(row) * V
+                            : q + static_cast<int64_t>(row - np) * V;
+  __shared__ float2 s_c[kSampleChunks];
+  block_chunk_stats<VEC>(x, V, s_c);
+  if (threadIdx.x < 32) {
+    const float2 cs = s_c[threadIdx.x];
+    const float2 r = merge_chunk_stats(cs);
+    if (threadIdx.x == 0) stats[row] = r;
+    if (row < np && row % (k + 1) == k)
+      bonus_chunks[static_cast<int64_t>(row / (k + 1)) * kSampleChunks + threadIdx.x] = cs;
   }
 }
 
 // The row a sequence samples from, in probability space: the residual
 // max(0, p(v) - q(v)) after a rejection, or p(v) itself for the bonus token
-// (q == null).  One inline function, so every kernel computes the same values.
+// (q == null).  One inline definition, so every kernel computes the same values.
 struct SampleRow {
   const float* p;
   const float* q;
   float mp, izp, mq, izq;   // row max * log2 e and 1 / sum, target and draft
-  __device__ __forceinline__ float value(float lp, float lq) const {
-    const float pv = scaled_exp(lp, mp) * izp;
-    if (q == nullptr) return pv;
-    return fmaxf(pv - scaled_exp(lq, mq) * izq, 0.f);
+  __device__ __forceinline__ float prob(float lp) const { return scaled_exp(lp, mp) * izp; }
+  __device__ __forceinline__ float resid(float pv, float lq) const {
+    return q == nullptr ? pv : fmaxf(pv - scaled_exp(lq, mq) * izq, 0.f);
   }
+  __device__ __forceinline__ float value(float lp, float lq) const { return resid(prob(lp), lq); }
   __device__ __forceinline__ float at(int v) const {
     return value(__ldg(p + v), q != nullptr ? __ldg(q + v) : 0.f);
   }
@@ -158,12 +211,6 @@ __device__ __forceinline__ SampleRow sample_row(const float* p, const float* q, 
     row.izq = 1.f / sq.y;
   }
   return row;
-}
-
-// Contiguous chunk `c` of a row of V tokens: [lo, hi).  The chunk length is a
-// multiple of 4 so float4 loads stay aligned when V is.
-__device__ __forceinline__ int chunk_len(int V) {
-  return ((V + kSampleChunks - 1) / kSampleChunks + 3) & ~3;
 }
 
 // One warp per sequence: the k ratio tests.  Draft x_i is accepted iff
@@ -234,9 +281,11 @@ __device__ __forceinline__ double2 block_sum2(double x, double y) {
   return t;
 }
 
-// One CTA per (sequence, chunk): the sums over the chunk of the residual row
-// max(0, p_a - q_a) and of p_a itself (the fallback when the residual
-// vanishes), or of p_k twice for the bonus row.  Coalesced 16-byte loads.
+// One CTA per (sequence, chunk) of a sequence that rejected a draft: the sums
+// over the chunk of the residual max(0, p_a - q_a) and of p_a itself (the
+// fallback when the residual vanishes).  Sequences that accepted every draft
+// sample the bonus row p_k, whose chunk masses the row statistics already
+// hold: their CTAs return at once.  Coalesced 16-byte loads.
 template <bool VEC>
 __global__ void __launch_bounds__(256)
     chunk_sum_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
@@ -246,158 +295,259 @@ __global__ void __launch_bounds__(256)
   const int c = blockIdx.x - n * kSampleChunks;
   const int tid = threadIdx.x;
   const int a = __ldg(accept + n);
+  if (a == k) return;
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, false);
-  const SampleRow prow = sample_row(p, q, stats, N, k, V, n, a, true);
   const int CL = chunk_len(V);
   const int lo = min(c * CL, V), hi = min(lo + CL, V);
   float sr = 0.f, sp = 0.f;
   if (VEC) {
     const float4* p4 = reinterpret_cast<const float4*>(row.p + lo);
-    const float4* q4 = row.q != nullptr ? reinterpret_cast<const float4*>(row.q + lo) : nullptr;
+    const float4* q4 = reinterpret_cast<const float4*>(row.q + lo);
     const int n4 = (hi - lo) >> 2;
+    const float neg_inf = -__builtin_huge_valf();
     for (int b = tid; b < n4; b += 4 * 256) {
       float4 lp[4], lq[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = b + j * 256;
-        lp[j] = i < n4 ? p4[i] : make_float4(-__builtin_huge_valf(), -__builtin_huge_valf(),
-                                              -__builtin_huge_valf(), -__builtin_huge_valf());
-        lq[j] = (q4 != nullptr && i < n4) ? q4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        lp[j] = i < n4 ? p4[i] : make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
+        lq[j] = i < n4 ? q4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        sr += ((row.value(lp[j].x, lq[j].x) + row.value(lp[j].y, lq[j].y)) +
-               (row.value(lp[j].z, lq[j].z) + row.value(lp[j].w, lq[j].w)));
-        sp += ((prow.value(lp[j].x, 0.f) + prow.value(lp[j].y, 0.f)) +
-               (prow.value(lp[j].z, 0.f) + prow.value(lp[j].w, 0.f)));
+        const float px = row.prob(lp[j].x), py = row.prob(lp[j].y);
+        const float pz = row.prob(lp[j].z), pw = row.prob(lp[j].w);
+        sr += (row.resid(px, lq[j].x) + row.resid(py, lq[j].y)) +
+              (row.resid(pz, lq[j].z) + row.resid(pw, lq[j].w));
+        sp += (px + py) + (pz + pw);
       }
     }
   } else {
     for (int v = lo + tid; v < hi; v += 256) {
-      const float lp = __ldg(row.p + v);
-      sr += row.value(lp, row.q != nullptr ? __ldg(row.q + v) : 0.f);
-      sp += prow.value(lp, 0.f);
+      const float pv = row.prob(__ldg(row.p + v));
+      sr += row.resid(pv, __ldg(row.q + v));
+      sp += pv;
     }
   }
   const double2 t = block_sum2<256>(static_cast<double>(sr), static_cast<double>(sp));
   if (tid == 0) chunk_sums[blockIdx.x] = t;
 }
 
-// One CTA per sequence: inverse CDF in token-id order.  The 32 chunk sums
-// (loaded in parallel) give the chunk holding u * Z; that chunk's residual
-// values are computed once into shared memory with coalesced loads, cut into
-// contiguous runs, one per thread, whose fp64 sums are prefix-summed in thread
-// order; the thread whose run spans the target walks it to the token.
+// Warp-wide, lane c holding chunk c's mass v >= 0 (fp64): the chunk where the
+// inverse CDF of u lands -- the first whose inclusive prefix (token order)
+// exceeds u * Z, Z the last prefix; the last chunk with mass if rounding puts
+// none past it; chunk 0 if every mass is 0 -- and the target's offset into it.
+__device__ __forceinline__ void choose_chunk(double v, double u, int lane, int& chunk, double& tgt) {
+  double incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const double target = u * __shfl_sync(0xffffffffu, incl, 31);
+  const unsigned over = __ballot_sync(0xffffffffu, incl > target);
+  const unsigned pos = __ballot_sync(0xffffffffu, v > 0.0);
+  chunk = over != 0u ? __ffs(over) - 1 : (pos != 0u ? 31 - __clz(pos) : 0);
+  const double prev = __shfl_sync(0xffffffffu, incl, chunk > 0 ? chunk - 1 : 0);
+  tgt = target - (chunk > 0 ? prev : 0.0);
+}
+
 constexpr int kPickThreads = 256;
 constexpr int kPickMaxChunk = 8192;    // chunk values staged in shared memory (V <= 262,144)
+static_assert(kPickThreads == kStatThreads, "the fused bonus sampler runs both phases in one CTA");
 
+struct PickSmem {
+  float r[kPickMaxChunk];          // the chunk's values (16-byte aligned: first member)
+  double warp_tot[kPickThreads / 32];
+  int owner, last, pick;
+};
+
+// Block-wide inverse CDF inside chunk [lo, hi) of `row`: the first token whose
+// running mass exceeds tgt, where the chunk is cut into contiguous per-thread
+// runs summed in fp32 and prefix-summed across runs in fp64 (token order).
+// The run holding the target is the last non-empty run whose exclusive prefix
+// is <= tgt (thread 0's is 0, so one always is); its thread walks it.  When
+// rounding leaves the target past that run, the run's last token with mass is
+// taken, else the chunk's.  The chunk's values are computed once into shared
+// memory with coalesced loads.  Every thread returns the token.
+template <bool VEC>
+__device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo, int hi, double tgt,
+                                                   PickSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int len = hi - lo;
+  const bool staged = len <= kPickMaxChunk;
+  if (tid == 0) {
+    sm.owner = -1;
+    sm.last = -1;
+    sm.pick = -1;
+  }
+  if (staged) {
+    if (VEC) {
+      const float4* p4 = reinterpret_cast<const float4*>(row.p + lo);
+      const float4* q4 = row.q != nullptr ? reinterpret_cast<const float4*>(row.q + lo) : nullptr;
+      float4* r4 = reinterpret_cast<float4*>(sm.r);
+      const int n4 = len >> 2;
+      for (int b = tid; b < n4; b += 4 * kPickThreads) {
+        float4 lp[4], lq[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = b + j * kPickThreads;
+          lp[j] = i < n4 ? __ldg(p4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          lq[j] = (q4 != nullptr && i < n4) ? __ldg(q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = b + j * kPickThreads;
+          if (i < n4)
+            r4[i] = make_float4(row.value(lp[j].x, lq[j].x), row.value(lp[j].y, lq[j].y),
+                                row.value(lp[j].z, lq[j].z), row.value(lp[j].w, lq[j].w));
+        }
+      }
+    } else {
+      for (int v = tid; v < len; v += kPickThreads) sm.r[v] = row.at(lo + v);
+    }
+  }
+  __syncthreads();
+  auto value = [&](int v) -> float { return staged ? sm.r[v - lo] : row.at(v); };
+  const int E = (len + kPickThreads - 1) / kPickThreads;
+  const int r0 = min(lo + tid * E, hi), r1 = min(r0 + E, hi);
+  float part = 0.f;
+  int my_last = -1;
+  for (int v = r0; v < r1; ++v) {
+    const float r = value(v);
+    part += r;
+    if (r > 0.f) my_last = v;
+  }
+  // Exclusive fp64 prefix of the run sums in thread order.
+  double incl = static_cast<double>(part);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.0;
+  if (lane == 31) sm.warp_tot[warp] = incl;
+  if (my_last >= 0) atomicMax(&sm.last, my_last);
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) excl += sm.warp_tot[w];
+  if (r0 < r1 && excl <= tgt) atomicMax(&sm.owner, tid);
+  __syncthreads();
+  if (tid == sm.owner) {
+    const double rem = tgt - excl;
+    float run = 0.f;
+    int pick = -1;
+    for (int v = r0; v < r1; ++v) {
+      const float r = value(v);
+      run += r;
+      if (r > 0.f && static_cast<double>(run) > rem) {
+        pick = v;
+        break;
+      }
+    }
+    sm.pick = pick >= 0 ? pick : my_last;
+  }
+  __syncthreads();
+  int tok = sm.pick >= 0 ? sm.pick : (sm.last >= 0 ? sm.last : lo);
+  return tok < hi ? tok : hi - 1;
+}
+
+// One CTA per sequence after the ratio tests: the 32 chunk masses (the
+// residual's, or p_a's when the residual vanishes, or the bonus row's from its
+// chunk statistics) locate the chunk holding u * Z; that chunk is scanned in
+// token-id order.
+template <bool VEC>
 __global__ void __launch_bounds__(kPickThreads)
     pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
-                uint64_t seed, uint32_t offset, uint32_t u_stream, int u_pos,
-                const float2* __restrict__ stats,
-                const int32_t* __restrict__ accept, const double2* __restrict__ chunk_sums,
-                int32_t* __restrict__ out_tokens) {
-  __shared__ double2 s_cs[kSampleChunks];
-  __shared__ double s_excl[kPickThreads + 1];
-  __shared__ float s_r[kPickMaxChunk];
-  __shared__ int s_chunk, s_use_p, s_pick, s_last;
+                uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
+                const float2* __restrict__ bonus_chunks, const int32_t* __restrict__ accept,
+                const double2* __restrict__ chunk_sums, int32_t* __restrict__ out_tokens) {
+  __shared__ __align__(16) PickSmem sm;
+  __shared__ int s_chunk, s_use_p;
   __shared__ double s_tgt;
   const int n = blockIdx.x;
   const int tid = threadIdx.x;
   const int a = __ldg(accept + n);
-  if (tid < kSampleChunks) s_cs[tid] = chunk_sums[static_cast<int64_t>(n) * kSampleChunks + tid];
-  __syncthreads();
-  if (tid == 0) {
-    double zr = 0.0;
-    for (int c = 0; c < kSampleChunks; ++c) zr += s_cs[c].x;
+  if (tid < 32) {
+    double2 cs;
+    if (a == k) {
+      const double v = chunk_mass(bonus_chunks[static_cast<int64_t>(n) * kSampleChunks + tid],
+                                  stats[static_cast<int64_t>(n) * (k + 1) + k]);
+      cs = make_double2(v, v);
+    } else {
+      cs = chunk_sums[static_cast<int64_t>(n) * kSampleChunks + tid];
+    }
+    double zr = cs.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zr += __shfl_xor_sync(0xffffffffu, zr, o);
     const bool use_p = (a == k) || !(zr > 0.0);
-    double Z = 0.0;
-    for (int c = 0; c < kSampleChunks; ++c) Z += use_p ? s_cs[c].y : s_cs[c].x;
-    // the uniform of counter (n, position, stream, offset): position a on the
-    // RESAMPLE stream for verification, the draft step on the DRAFT stream
-    const double target =
-        static_cast<double>(philox_uniform(seed, offset, n, u_pos >= 0 ? u_pos : a, u_stream)) * Z;
-    // First chunk whose inclusive prefix exceeds the target, else the last
-    // chunk with positive mass.
-    double run = 0.0, base = 0.0, last_base = 0.0;
-    int pick = -1, last = 0;
-    for (int c = 0; c < kSampleChunks; ++c) {
-      const double v = use_p ? s_cs[c].y : s_cs[c].x;
-      if (v > 0.0) {
-        last = c;
-        last_base = run;
-      }
-      if (pick < 0 && run + v > target) {
-        pick = c;
-        base = run;
-      }
-      run += v;
+    double v = use_p ? cs.y : cs.x;
+    v = v > 0.0 ? v : 0.0;
+    // the uniform of counter (n, a, RESAMPLE, offset)
+    const double u = static_cast<double>(philox_uniform(seed, offset, n, a, kStreamResample));
+    int chunk;
+    double tgt;
+    choose_chunk(v, u, tid, chunk, tgt);
+    if (tid == 0) {
+      s_chunk = chunk;
+      s_use_p = use_p ? 1 : 0;
+      s_tgt = tgt;
     }
-    if (pick < 0) {
-      pick = last;
-      base = last_base;
-    }
-    s_chunk = pick;
-    s_use_p = use_p ? 1 : 0;
-    s_tgt = target - base;
-    s_pick = 0x7fffffff;
-    s_last = -1;
   }
   __syncthreads();
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, s_use_p != 0);
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
-  const int len = hi - lo;
-  const bool staged = len <= kPickMaxChunk;
-  if (staged) {
-    for (int v = tid; v < len; v += kPickThreads) s_r[v] = row.at(lo + v);
-    __syncthreads();
-  }
-  auto value = [&](int v) -> float { return staged ? s_r[v - lo] : row.at(v); };
-  const int E = (len + kPickThreads - 1) / kPickThreads;
-  const int r0 = min(lo + tid * E, hi), r1 = min(r0 + E, hi);
-  double part = 0.0;
-  int my_last = -1;
-  for (int v = r0; v < r1; ++v) {
-    const float r = value(v);
-    part += static_cast<double>(r);
-    if (r > 0.f) my_last = v;
-  }
-  s_excl[tid] = part;
-  if (my_last >= 0) atomicMax(&s_last, my_last);
-  __syncthreads();
-  if (tid == 0) {
-    // Exclusive prefix in thread order, sequential so it is monotone.
-    double run = 0.0;
-    for (int t = 0; t < kPickThreads; ++t) {
-      const double v = s_excl[t];
-      s_excl[t] = run;
-      run += v;
+  const int tok = block_pick_in_chunk<VEC>(row, lo, hi, s_tgt, sm);
+  if (tid == 0) out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
+}
+
+// k = 0: one CTA per sequence samples one token from softmax(p_n) in a single
+// kernel -- the row's chunk statistics (one streaming pass), the chunk holding
+// u * Z from them, then that chunk's inverse CDF.  The uniform is the one of
+// counter (n, u_pos, u_stream, offset).  Writes n_accepted[n] = 0.
+template <bool VEC>
+__global__ void __launch_bounds__(kStatThreads)
+    bonus_sample_kernel(const float* __restrict__ p, int V, uint64_t seed, uint32_t offset,
+                        uint32_t u_stream, int u_pos, int32_t* __restrict__ out_tokens,
+                        int32_t* __restrict__ n_accepted) {
+  __shared__ __align__(16) PickSmem sm;
+  __shared__ float2 s_c[kSampleChunks];
+  __shared__ float2 s_row;
+  __shared__ int s_chunk;
+  __shared__ double s_tgt;
+  const int n = blockIdx.x;
+  const int tid = threadIdx.x;
+  const float* x = p + static_cast<int64_t>(n) * V;
+  block_chunk_stats<VEC>(x, V, s_c);
+  if (tid < 32) {
+    const float2 cs = s_c[tid];
+    float2 r = merge_chunk_stats(cs);
+    r.x = __shfl_sync(0xffffffffu, r.x, 0);
+    r.y = __shfl_sync(0xffffffffu, r.y, 0);
+    const double u = static_cast<double>(philox_uniform(seed, offset, n, u_pos, u_stream));
+    int chunk;
+    double tgt;
+    choose_chunk(chunk_mass(cs, r), u, tid, chunk, tgt);
+    if (tid == 0) {
+      s_chunk = chunk;
+      s_tgt = tgt;
+      s_row = r;
+      n_accepted[n] = 0;
     }
-    s_excl[kPickThreads] = __longlong_as_double(0x7ff0000000000000LL);   // +inf
   }
   __syncthreads();
-  const double tgt = s_tgt;
-  if (s_excl[tid] <= tgt && tgt < s_excl[tid + 1]) {
-    double run = s_excl[tid];
-    int pick = -1;
-    for (int v = r0; v < r1; ++v) {
-      const float r = value(v);
-      run += static_cast<double>(r);
-      if (r > 0.f && run > tgt) {
-        pick = v;
-        break;
-      }
-    }
-    if (pick < 0) pick = my_last;
-    if (pick >= 0) atomicMin(&s_pick, pick);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int tok = s_pick != 0x7fffffff ? s_pick : s_last;
-    if (tok < 0) tok = lo < V ? lo : V - 1;
-    out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
-  }
+  SampleRow row;
+  row.p = x;
+  row.q = nullptr;
+  row.mp = s_row.x * kLog2e;
+  row.izp = 1.f / s_row.y;
+  row.mq = 0.f;
+  row.izq = 0.f;
+  const int CL = chunk_len(V);
+  const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
+  const int tok = block_pick_in_chunk<VEC>(row, lo, hi, s_tgt, sm);
+  if (tid == 0) out_tokens[n] = tok;
 }
 
 }  // namespace
@@ -409,7 +559,8 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
   L.stats_off = 256;
   L.accept_off = L.stats_off + al(static_cast<size_t>(N) * (2 * k + 1) * sizeof(float2));
   L.chunk_off = L.accept_off + al(static_cast<size_t>(N) * sizeof(int32_t));
-  L.total = L.chunk_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(double2));
+  L.bonus_off = L.chunk_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(double2));
+  L.total = L.bonus_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(float2));
   return L;
 }
 
@@ -424,13 +575,25 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   float2* stats = reinterpret_cast<float2*>(w + L.stats_off);
   int32_t* accept = reinterpret_cast<int32_t*>(w + L.accept_off);
   double2* chunks = reinterpret_cast<double2*>(w + L.chunk_off);
-  const int rows = N * (2 * k + 1);
+  float2* bonus = reinterpret_cast<float2*>(w + L.bonus_off);
   const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                    (k == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
+  if (k == 0) {
+    const int pos = u_pos >= 0 ? u_pos : 0;
+    if (vec) {
+      bonus_sample_kernel<true><<<N, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, out_tokens,
+                                                                n_accepted);
+    } else {
+      bonus_sample_kernel<false><<<N, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, out_tokens,
+                                                                 n_accepted);
+    }
+    return cudaGetLastError();
+  }
+  const int rows = N * (2 * k + 1);
   if (vec) {
-    row_stats_kernel<true><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats);
+    row_stats_kernel<true><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, bonus);
   } else {
-    row_stats_kernel<false><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats);
+    row_stats_kernel<false><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, bonus);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -448,8 +611,13 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  pick_kernel<<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, u_stream, u_pos, stats, accept,
-                                              chunks, out_tokens);
+  if (vec) {
+    pick_kernel<true><<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks,
+                                                      out_tokens);
+  } else {
+    pick_kernel<false><<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks,
+                                                       out_tokens);
+  }
   return cudaGetLastError();
 }
 

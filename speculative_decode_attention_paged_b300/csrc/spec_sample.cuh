@@ -16,16 +16,18 @@ struct SpecWorkspaceLayout {
   size_t stats_off;   // float2 [N][2k+1]: (row max, sum of exp(x - max))
   size_t accept_off;  // int32 [N]: accepted count a = index of the row sampled from
   size_t chunk_off;   // double2 [N][kSampleChunks]: (residual sum, target-row sum) per chunk
+  size_t bonus_off;   // float2 [N][kSampleChunks]: (max, sum) per chunk of the bonus row p_k
   size_t total;
 };
 
 SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k);
 
-// Enqueue the four sampler kernels.  `ws` is the caller's workspace laid out
-// by spec_workspace_layout(N, k).  The final inverse CDF draws the Philox
-// uniform of counter (n, u_pos, u_stream, offset); u_pos < 0 means the
-// sequence's accepted count (verification: stream RESAMPLE).  With k = 0 and
-// no draft rows this samples one token from softmax(p) per sequence.
+// Enqueue the sampler kernels.  `ws` is the caller's workspace laid out by
+// spec_workspace_layout(N, k).  With k > 0 the final inverse CDF draws the
+// Philox uniform of counter (n, a, RESAMPLE, offset), a the accepted count.
+// With k = 0 (no draft rows) one token is sampled from softmax(p) per sequence
+// with the uniform of counter (n, u_pos, u_stream, offset), u_pos < 0 meaning
+// 0, and n_accepted is set to 0.
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                int V, uint64_t seed, uint32_t offset, void* ws,
                                int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
