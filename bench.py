@@ -690,7 +690,22 @@ def run_sampler(args):
         nbytes = N * (2 * sc.k + 1) * sc.vocab * 4 + N * (2 * sc.k + 2) * 4
         reached = np.array([(a >= i).sum() for i in range(sc.k)])
         accepted = np.array([(a > i).sum() for i in range(sc.k)])
+        # the sequential sampler on the same inputs: rows up to each first rejection only
+        out_s = torch.empty_like(out)
+        nacc_s = torch.empty_like(nacc)
+        t_seq = _timed(lambda: s3r.s3r_spec_sample_sequential(inp.p_logits, inp.q_logits, inp.draft_tokens,
+                                                              sc.philox_seed, 0, out_s, nacc_s, ws),
+                       args.steps, args.warmup)
+        ws.check()
+        if not (torch.equal(out_s, out) and torch.equal(nacc_s, nacc)):
+            raise RuntimeError("sequential sampler differs from the parallel sampler")
+        rows_read = int(np.where(a < sc.k, 2 * (a + 1), 2 * sc.k + 1).sum())
+        seq_bytes = rows_read * sc.vocab * 4
+        sequential = {"ms": t_seq, "rows_read": rows_read, "rows_total": N * (2 * sc.k + 1),
+                      "gb": seq_bytes / 1e9, "gbs": seq_bytes / (t_seq * 1e-3) / 1e9,
+                      "speedup_vs_parallel": t / t_seq}
         res[str(sigma)] = {"ms": t, "gb": nbytes / 1e9, "gbs": nbytes / (t * 1e-3) / 1e9,
+                           "sequential": sequential,
                            "mean_accepted": float(a.mean()), "mean_emitted": float((a + 1).mean()),
                            "per_position_acceptance": [float(x) for x in accepted / np.maximum(reached, 1)],
                            "accepted_histogram": np.bincount(a, minlength=sc.k + 1).tolist(),

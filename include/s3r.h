@@ -31,8 +31,8 @@
  *  - Workspace: one caller-allocated device buffer of at least the size that
  *    the *_workspace_size() queries return, 256-byte aligned.  Its first 256
  *    bytes hold the sticky error word; the attention calls also keep
- *    per-(sequence, KV head) arrival counters in it, which every call leaves
- *    at zero.  Zero the whole buffer once with s3r_workspace_init() after
+ *    per-(sequence, KV head) arrival counters in it, and the samplers
+ *    per-sequence ones, which every call leaves at zero.  Zero the whole buffer once with s3r_workspace_init() after
  *    allocation, and again after a call reported S3R_DEVERR_TIMEOUT.  Calls
  *    that share a workspace must be ordered (same stream or event-ordered).
  *  - KV cache layout: bf16 pools [num_phys_pages][num_kv_heads][16][128]
@@ -234,6 +234,26 @@ S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
                            uint64_t seed, uint64_t offset, int32_t* out_tokens,
                            int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Exact speculative sampling with the ratio tests taken one draft position at
+ * a time: the rows of a sequence after its first rejection (p_j and q_j for
+ * j > a) are never read, and the bonus row p_{k+1} only when all k drafts
+ * were accepted.  The drafts are tested in order and sampling stops at the
+ * first rejection (wispaper.ai, "S3R drafts sparsely and verifies densely";
+ * rebasdaily.com, "草稿可以稀疏，交卷必须完整"), so the skipped rows cannot
+ * change the result.
+ *
+ * Same arguments, semantics, results (bit for bit) and workspace size as
+ * s3r_spec_sample.  It enqueues k + 3 kernels instead of 4 and reads about
+ * (2 E[a] + 2) / (2k + 1) of the logit bytes, E[a] the mean accepted count.
+ * Its workspace must hold zeroed arrival counters (s3r_workspace_init once
+ * after allocation); every call leaves them at zero.
+ */
+S3R_API s3r_status s3r_spec_sample_sequential(const float* p_logits, const float* q_logits,
+                                      const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
+                                      uint64_t seed, uint64_t offset, int32_t* out_tokens,
+                                      int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes for s3r_sample_draft_tokens with n sequences (host). */
 S3R_API s3r_status s3r_sample_draft_workspace_size(int32_t n, size_t* bytes);
 
@@ -273,7 +293,7 @@ S3R_API s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32
  *                 call's device error bits (the S3R_DEVERR_* values)
  * Returns S3R_ERR_UNSUPPORTED, before enqueuing anything, when
  * s3r_spec_sample_workspace_size(n, k) exceeds S3R_NOALLOC_SCRATCH_BYTES
- * (for example n = 2048 with k = 8 needs 1,859,840 bytes and fits).
+ * (for example n = 2048 with k = 8 needs 1,868,032 bytes and fits).
  * The first call on each device looks up the array's device address (a
  * one-time set-up per device, with that device current): make that first
  * call before any stream capture.  Every call on a device shares the one

@@ -29,6 +29,7 @@ __all__ = [
     "s3r_verify_attn",
     "s3r_select_draft_pages",
     "s3r_spec_sample",
+    "s3r_spec_sample_sequential",
     "s3r_spec_sample_noalloc",
     "s3r_sample_draft_workspace_size",
     "s3r_sample_draft_tokens",
@@ -100,6 +101,8 @@ _SIG = {
                                               _I32, _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64, _P, _P,
                                        _P, ctypes.c_size_t, _P]),
+    "s3r_spec_sample_sequential": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
+                                                  _P, _P, _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
                                                _P, _P, _P, _P]),
     "s3r_sample_draft_workspace_size": (ctypes.c_int, [_I32, ctypes.POINTER(ctypes.c_size_t)]),
@@ -296,6 +299,22 @@ def s3r_spec_sample(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, 
     n, k1, V = p_logits.shape
     _call("s3r_spec_sample", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1), _I32(V),
           ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), ws.ptr(),
+          ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return out_tokens, n_accepted
+
+
+def s3r_spec_sample_sequential(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, n_accepted,
+                               ws: Workspace, stream=None):
+    """s3r_spec_sample with the ratio tests one position at a time, reading no
+    row after a sequence's first rejection; the same results bit for bit."""
+    _need(p_logits, torch.float32, "p_logits")
+    _need(q_logits, torch.float32, "q_logits")
+    _need(draft_tokens, torch.int32, "draft_tokens")
+    _need(out_tokens, torch.int32, "out_tokens")
+    _need(n_accepted, torch.int32, "n_accepted")
+    n, k1, V = p_logits.shape
+    _call("s3r_spec_sample_sequential", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1),
+          _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), ws.ptr(),
           ctypes.c_size_t(ws.nbytes), _stream(stream))
     return out_tokens, n_accepted
 

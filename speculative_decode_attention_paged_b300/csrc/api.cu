@@ -320,10 +320,9 @@ s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t* sel_len
                                        static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
 }
 
-s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
-                           const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
-                           uint64_t seed, uint64_t offset, int32_t* out_tokens,
-                           int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
+static s3r_status check_spec_sample(const float* p_logits, const float* q_logits, const int32_t* draft_tokens,
+                                     int32_t n, int32_t k, int32_t vocab, uint64_t offset, int32_t* out_tokens,
+                                     int32_t* n_accepted, void* ws, size_t ws_bytes) {
   if (n < 0 || k < 0 || vocab <= 0) return S3R_ERR_INVALID_ARG;
   if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
   if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
@@ -335,9 +334,31 @@ s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
   if (n == 0) return S3R_OK;
   if (p_logits == nullptr || out_tokens == nullptr || n_accepted == nullptr) return S3R_ERR_INVALID_ARG;
   if (k > 0 && (q_logits == nullptr || draft_tokens == nullptr)) return S3R_ERR_INVALID_ARG;
+  return S3R_OK;
+}
+
+s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
+                           const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
+                           uint64_t seed, uint64_t offset, int32_t* out_tokens,
+                           int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
+  const s3r_status st = check_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens,
+                                          n_accepted, ws, ws_bytes);
+  if (st != S3R_OK || n == 0) return st;
   return to_status(launch_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
                                       static_cast<uint32_t>(offset), ws, out_tokens, n_accepted,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+s3r_status s3r_spec_sample_sequential(const float* p_logits, const float* q_logits,
+                                      const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
+                                      uint64_t seed, uint64_t offset, int32_t* out_tokens,
+                                      int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
+  const s3r_status st = check_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens,
+                                          n_accepted, ws, ws_bytes);
+  if (st != S3R_OK || n == 0) return st;
+  return to_status(launch_spec_sample_sequential(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
+                                                 static_cast<uint32_t>(offset), ws, out_tokens, n_accepted,
+                                                 static_cast<cudaStream_t>(stream)));
 }
 
 s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, uint64_t seed,

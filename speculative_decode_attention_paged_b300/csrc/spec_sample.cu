@@ -25,7 +25,11 @@
 //               (fp32 sums over contiguous per-thread runs, fp64 prefix across
 //               runs) to find the token.
 // With k = 0 there is nothing to test and the row is its own bonus row:
-// bonus_sample does row_stats and pick for one sequence in one CTA.
+// bonus_sample streams each row with 4 CTAs, the last of which merges the
+// chunk statistics and picks the token.
+// The sequential variant replaces row_stats + accept by k + 1 launches of
+// seq_step, one per position, which read a sequence's rows only up to its
+// first rejection; chunk_sum and pick follow as above.
 
 #include <cfloat>
 
@@ -53,6 +57,10 @@ __device__ __forceinline__ void merge_stats(float& m, float& z, float m2, float 
   z = z * a + z2 * b;
   m = mn;
 }
+
+// A row is also split over kRowParts CTAs of 8 warps, one warp per chunk.
+constexpr int kRowParts = 4;
+static_assert(kSampleChunks == kRowParts * (kStatThreads / 32), "one warp per chunk");
 
 // Contiguous chunk `c` of a row of V tokens: [lo, hi).  The chunk length is a
 // multiple of 4 so float4 loads stay aligned when V is.
@@ -213,6 +221,14 @@ __device__ __forceinline__ SampleRow sample_row(const float* p, const float* q, 
   return row;
 }
 
+// The ratio test of one drafted token x: rejected unless u < p(x) / q(x), the
+// ratio formed in fp64 from the fp32 logits p(x), q(x) and the rows' (max, sum).
+__device__ __forceinline__ bool ratio_rejects(float lp, float lq, float2 sp, float2 sq, float u) {
+  const double e = (static_cast<double>(lp) - sp.x) - (static_cast<double>(lq) - sq.x);
+  const double ratio = exp2(e * kLog2eD) * static_cast<double>(sq.y) / static_cast<double>(sp.y);
+  return !(static_cast<double>(u) < ratio);
+}
+
 // One warp per sequence: the k ratio tests.  Draft x_i is accepted iff
 // u(n, i-1, ACCEPT) < p_i(x_i) / q_i(x_i); the ratio is formed in fp64 from the
 // fp32 logits and row statistics.  Writes a = index of the first rejection
@@ -236,14 +252,11 @@ __global__ void __launch_bounds__(256)
         report_error(err, S3R_DEVERR_BAD_TOKEN);
         rej = true;
       } else {
-        const float lp = __ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x);
-        const float lq = __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x);
-        const float2 sp = stats[static_cast<int64_t>(n) * (k + 1) + i];
-        const float2 sq = stats[np_rows + static_cast<int64_t>(n) * k + i];
-        const double e = (static_cast<double>(lp) - sp.x) - (static_cast<double>(lq) - sq.x);
-        const double ratio = exp2(e * kLog2eD) * static_cast<double>(sq.y) / static_cast<double>(sp.y);
-        const float u = philox_uniform(seed, offset, n, i, kStreamAccept);
-        rej = !(static_cast<double>(u) < ratio);
+        rej = ratio_rejects(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x),
+                            __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x),
+                            stats[static_cast<int64_t>(n) * (k + 1) + i],
+                            stats[np_rows + static_cast<int64_t>(n) * k + i],
+                            philox_uniform(seed, offset, n, i, kStreamAccept));
       }
     }
     const unsigned b = __ballot_sync(0xffffffffu, rej);
@@ -260,77 +273,85 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// Block-wide sum of two doubles (fixed reduction order); result in thread 0.
-template <int THREADS>
-__device__ __forceinline__ double2 block_sum2(double x, double y) {
-  __shared__ double2 s_w[THREADS / 32];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    x += __shfl_xor_sync(0xffffffffu, x, o);
-    y += __shfl_xor_sync(0xffffffffu, y, o);
-  }
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = make_double2(x, y);
-  __syncthreads();
-  double2 t = make_double2(0.0, 0.0);
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < THREADS / 32; ++w) {
-      t.x += s_w[w].x;
-      t.y += s_w[w].y;
-    }
-  }
-  return t;
+// s += x with Kahan compensation c (the sum is s - c).
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = x - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
 }
 
-// One CTA per (sequence, chunk) of a sequence that rejected a draft: the sums
-// over the chunk of the residual max(0, p_a - q_a) and of p_a itself (the
-// fallback when the residual vanishes).  Sequences that accepted every draft
-// sample the bonus row p_k, whose chunk masses the row statistics already
-// hold: their CTAs return at once.  Coalesced 16-byte loads.
+// One warp per chunk of a sequence that rejected a draft (kRowParts CTAs of 8
+// warps per sequence): the sums over the chunk of the residual
+// max(0, p_a - q_a) and of p_a itself (the fallback when the residual
+// vanishes), fp32 over each 16-value batch, compensated across batches, fp64
+// across lanes.  Sequences that accepted every draft sample the bonus row
+// p_k, whose chunk masses the row statistics already hold: their CTAs return
+// at once.  Coalesced 16-byte loads.
 template <bool VEC>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kStatThreads)
     chunk_sum_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
                      const float2* __restrict__ stats, const int32_t* __restrict__ accept,
                      double2* __restrict__ chunk_sums) {
-  const int n = blockIdx.x / kSampleChunks;
-  const int c = blockIdx.x - n * kSampleChunks;
-  const int tid = threadIdx.x;
+  const int n = blockIdx.x / kRowParts;
+  const int part = blockIdx.x - n * kRowParts;
   const int a = __ldg(accept + n);
   if (a == k) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, false);
   const int CL = chunk_len(V);
+  const int c = part * (kStatThreads / 32) + warp;
   const int lo = min(c * CL, V), hi = min(lo + CL, V);
-  float sr = 0.f, sp = 0.f;
+  float sr = 0.f, cr = 0.f, sp = 0.f, cp = 0.f;
   if (VEC) {
     const float4* p4 = reinterpret_cast<const float4*>(row.p + lo);
     const float4* q4 = reinterpret_cast<const float4*>(row.q + lo);
     const int n4 = (hi - lo) >> 2;
     const float neg_inf = -__builtin_huge_valf();
-    for (int b = tid; b < n4; b += 4 * 256) {
+    for (int base = 0; base < n4; base += 4 * 32) {
       float4 lp[4], lq[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int i = b + j * 256;
-        lp[j] = i < n4 ? p4[i] : make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
-        lq[j] = i < n4 ? q4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int i = base + j * 32 + lane;
+        lp[j] = i < n4 ? __ldcs(p4 + i) : make_float4(neg_inf, neg_inf, neg_inf, neg_inf);
+        lq[j] = i < n4 ? __ldcs(q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      float br = 0.f, bp = 0.f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float px = row.prob(lp[j].x), py = row.prob(lp[j].y);
         const float pz = row.prob(lp[j].z), pw = row.prob(lp[j].w);
-        sr += (row.resid(px, lq[j].x) + row.resid(py, lq[j].y)) +
+        br += (row.resid(px, lq[j].x) + row.resid(py, lq[j].y)) +
               (row.resid(pz, lq[j].z) + row.resid(pw, lq[j].w));
-        sp += (px + py) + (pz + pw);
+        bp += (px + py) + (pz + pw);
       }
+      kahan_add(sr, cr, br);
+      kahan_add(sp, cp, bp);
     }
   } else {
-    for (int v = lo + tid; v < hi; v += 256) {
-      const float pv = row.prob(__ldg(row.p + v));
-      sr += row.resid(pv, __ldg(row.q + v));
-      sp += pv;
+    for (int base = lo; base < hi; base += 4 * 32) {
+      float br = 0.f, bp = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = base + j * 32 + lane;
+        if (v < hi) {
+          const float pv = row.prob(__ldcs(row.p + v));
+          br += row.resid(pv, __ldcs(row.q + v));
+          bp += pv;
+        }
+      }
+      kahan_add(sr, cr, br);
+      kahan_add(sp, cp, bp);
     }
   }
-  const double2 t = block_sum2<256>(static_cast<double>(sr), static_cast<double>(sp));
-  if (tid == 0) chunk_sums[blockIdx.x] = t;
+  double dr = static_cast<double>(sr) - static_cast<double>(cr);
+  double dp = static_cast<double>(sp) - static_cast<double>(cp);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    dr += __shfl_xor_sync(0xffffffffu, dr, o);
+    dp += __shfl_xor_sync(0xffffffffu, dp, o);
+  }
+  if (lane == 0) chunk_sums[static_cast<int64_t>(n) * kSampleChunks + c] = make_double2(dr, dp);
 }
 
 // Warp-wide, lane c holding chunk c's mass v >= 0 (fp64): the chunk where the
@@ -353,11 +374,9 @@ __device__ __forceinline__ void choose_chunk(double v, double u, int lane, int& 
 }
 
 constexpr int kPickThreads = 256;
-constexpr int kPickMaxChunk = 8192;    // chunk values staged in shared memory (V <= 262,144)
-static_assert(kPickThreads == kStatThreads, "the fused bonus sampler runs both phases in one CTA");
+static_assert(kPickThreads == kStatThreads, "the bonus sampler runs both phases in one CTA");
 
 struct PickSmem {
-  float r[kPickMaxChunk];          // the chunk's values (16-byte aligned: first member)
   double warp_tot[kPickThreads / 32];
   int owner, last, pick;
 };
@@ -366,57 +385,38 @@ struct PickSmem {
 // running mass exceeds tgt, where the chunk is cut into contiguous per-thread
 // runs summed in fp32 and prefix-summed across runs in fp64 (token order).
 // The run holding the target is the last non-empty run whose exclusive prefix
-// is <= tgt (thread 0's is 0, so one always is); its thread walks it.  When
-// rounding leaves the target past that run, the run's last token with mass is
-// taken, else the chunk's.  The chunk's values are computed once into shared
-// memory with coalesced loads.  Every thread returns the token.
-template <bool VEC>
+// is <= tgt (thread 0's is 0, so one always is); its thread walks it again
+// (the same values, now from L1).  When rounding leaves the target past that
+// run, the run's last token with mass is taken, else the chunk's.  Nothing is
+// staged in shared memory, so kernels that stream rows before picking keep
+// their L1 for loads in flight.  Every thread returns the token.
 __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo, int hi, double tgt,
                                                    PickSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int len = hi - lo;
-  const bool staged = len <= kPickMaxChunk;
   if (tid == 0) {
     sm.owner = -1;
     sm.last = -1;
     sm.pick = -1;
   }
-  if (staged) {
-    if (VEC) {
-      const float4* p4 = reinterpret_cast<const float4*>(row.p + lo);
-      const float4* q4 = row.q != nullptr ? reinterpret_cast<const float4*>(row.q + lo) : nullptr;
-      float4* r4 = reinterpret_cast<float4*>(sm.r);
-      const int n4 = len >> 2;
-      for (int b = tid; b < n4; b += 4 * kPickThreads) {
-        float4 lp[4], lq[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = b + j * kPickThreads;
-          lp[j] = i < n4 ? __ldg(p4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-          lq[j] = (q4 != nullptr && i < n4) ? __ldg(q4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = b + j * kPickThreads;
-          if (i < n4)
-            r4[i] = make_float4(row.value(lp[j].x, lq[j].x), row.value(lp[j].y, lq[j].y),
-                                row.value(lp[j].z, lq[j].z), row.value(lp[j].w, lq[j].w));
-        }
-      }
-    } else {
-      for (int v = tid; v < len; v += kPickThreads) sm.r[v] = row.at(lo + v);
-    }
-  }
-  __syncthreads();
-  auto value = [&](int v) -> float { return staged ? sm.r[v - lo] : row.at(v); };
   const int E = (len + kPickThreads - 1) / kPickThreads;
   const int r0 = min(lo + tid * E, hi), r1 = min(r0 + E, hi);
   float part = 0.f;
   int my_last = -1;
-  for (int v = r0; v < r1; ++v) {
-    const float r = value(v);
-    part += r;
-    if (r > 0.f) my_last = v;
+  for (int v0 = r0; v0 < r1; v0 += 8) {
+    float lp[8], lq[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool in = v0 + j < r1;
+      lp[j] = in ? __ldg(row.p + v0 + j) : -__builtin_huge_valf();
+      lq[j] = (in && row.q != nullptr) ? __ldg(row.q + v0 + j) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float r = row.value(lp[j], lq[j]);
+      part += r;
+      if (r > 0.f) my_last = v0 + j;
+    }
   }
   // Exclusive fp64 prefix of the run sums in thread order.
   double incl = static_cast<double>(part);
@@ -428,8 +428,8 @@ __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo,
   double excl = __shfl_up_sync(0xffffffffu, incl, 1);
   if (lane == 0) excl = 0.0;
   if (lane == 31) sm.warp_tot[warp] = incl;
-  if (my_last >= 0) atomicMax(&sm.last, my_last);
   __syncthreads();
+  if (my_last >= 0) atomicMax(&sm.last, my_last);
   for (int w = 0; w < warp; ++w) excl += sm.warp_tot[w];
   if (r0 < r1 && excl <= tgt) atomicMax(&sm.owner, tid);
   __syncthreads();
@@ -438,7 +438,7 @@ __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo,
     float run = 0.f;
     int pick = -1;
     for (int v = r0; v < r1; ++v) {
-      const float r = value(v);
+      const float r = row.at(v);
       run += r;
       if (r > 0.f && static_cast<double>(run) > rem) {
         pick = v;
@@ -448,7 +448,7 @@ __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo,
     sm.pick = pick >= 0 ? pick : my_last;
   }
   __syncthreads();
-  int tok = sm.pick >= 0 ? sm.pick : (sm.last >= 0 ? sm.last : lo);
+  const int tok = sm.pick >= 0 ? sm.pick : (sm.last >= 0 ? sm.last : lo);
   return tok < hi ? tok : hi - 1;
 }
 
@@ -456,13 +456,12 @@ __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo,
 // residual's, or p_a's when the residual vanishes, or the bonus row's from its
 // chunk statistics) locate the chunk holding u * Z; that chunk is scanned in
 // token-id order.
-template <bool VEC>
 __global__ void __launch_bounds__(kPickThreads)
     pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
                 uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
                 const float2* __restrict__ bonus_chunks, const int32_t* __restrict__ accept,
                 const double2* __restrict__ chunk_sums, int32_t* __restrict__ out_tokens) {
-  __shared__ __align__(16) PickSmem sm;
+  __shared__ PickSmem sm;
   __shared__ int s_chunk, s_use_p;
   __shared__ double s_tgt;
   const int n = blockIdx.x;
@@ -498,30 +497,62 @@ __global__ void __launch_bounds__(kPickThreads)
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, s_use_p != 0);
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
-  const int tok = block_pick_in_chunk<VEC>(row, lo, hi, s_tgt, sm);
+  const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, sm);
   if (tid == 0) out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
 }
 
-// k = 0: one CTA per sequence samples one token from softmax(p_n) in a single
-// kernel -- the row's chunk statistics (one streaming pass), the chunk holding
-// u * Z from them, then that chunk's inverse CDF.  The uniform is the one of
-// counter (n, u_pos, u_stream, offset).  Writes n_accepted[n] = 0.
+// Rows split over CTAs: each of kRowParts CTAs streams 8 chunks of a row (one
+// warp per chunk) and stores their (max, sum) pairs; the CTA that arrives
+// last on the sequence's counter (the stores published by a fence before the
+// arrival) merges the pairs, acts for the sequence and resets the counter.
+// The chunk pairs and their merge are those of row_stats, so the row
+// statistics are bitwise the same.
+
+// This CTA's 8 chunks of row x into dst[kSampleChunks]; true in every thread
+// of the CTA that arrived last among `arrivals_expected` on *counter.
+template <bool VEC>
+__device__ __forceinline__ bool split_chunks_arrive(const float* __restrict__ x, int V, int part,
+                                                    float2* __restrict__ dst, int* counter,
+                                                    int arrivals_expected) {
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int CL = chunk_len(V);
+  const int c = part * (kStatThreads / 32) + warp;
+  const int lo = min(c * CL, V), hi = min(lo + CL, V);
+  const float2 s = warp_chunk_stats<VEC>(x, lo, hi, lane);
+  if (lane == 0) dst[c] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(counter, 1) == arrivals_expected - 1;
+  }
+  __syncthreads();
+  const bool last = s_last != 0;
+  if (last) __threadfence();
+  return last;
+}
+
+// k = 0: one token per sequence from softmax(p_n), kRowParts CTAs per row;
+// the last to arrive takes the chunk holding u * Z from the merged chunk
+// statistics and scans it.  The uniform is the one of counter
+// (n, u_pos, u_stream, offset).  Writes n_accepted[n] = 0.
 template <bool VEC>
 __global__ void __launch_bounds__(kStatThreads)
     bonus_sample_kernel(const float* __restrict__ p, int V, uint64_t seed, uint32_t offset,
-                        uint32_t u_stream, int u_pos, int32_t* __restrict__ out_tokens,
-                        int32_t* __restrict__ n_accepted) {
-  __shared__ __align__(16) PickSmem sm;
-  __shared__ float2 s_c[kSampleChunks];
+                        uint32_t u_stream, int u_pos, float2* __restrict__ chunks, int* __restrict__ arrivals,
+                        int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted) {
+  __shared__ PickSmem sm;
   __shared__ float2 s_row;
   __shared__ int s_chunk;
   __shared__ double s_tgt;
-  const int n = blockIdx.x;
+  const int n = blockIdx.x / kRowParts;
+  const int part = blockIdx.x - n * kRowParts;
   const int tid = threadIdx.x;
   const float* x = p + static_cast<int64_t>(n) * V;
-  block_chunk_stats<VEC>(x, V, s_c);
+  float2* cs_n = chunks + static_cast<int64_t>(n) * kSampleChunks;
+  if (!split_chunks_arrive<VEC>(x, V, part, cs_n, arrivals + n, kRowParts)) return;
   if (tid < 32) {
-    const float2 cs = s_c[tid];
+    const float2 cs = __ldcg(cs_n + tid);
     float2 r = merge_chunk_stats(cs);
     r.x = __shfl_sync(0xffffffffu, r.x, 0);
     r.y = __shfl_sync(0xffffffffu, r.y, 0);
@@ -533,6 +564,7 @@ __global__ void __launch_bounds__(kStatThreads)
       s_chunk = chunk;
       s_tgt = tgt;
       s_row = r;
+      arrivals[n] = 0;
       n_accepted[n] = 0;
     }
   }
@@ -546,8 +578,89 @@ __global__ void __launch_bounds__(kStatThreads)
   row.izq = 0.f;
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
-  const int tok = block_pick_in_chunk<VEC>(row, lo, hi, s_tgt, sm);
+  const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, sm);
   if (tid == 0) out_tokens[n] = tok;
+}
+
+// Step i of the sequential (early-exit) ratio tests.  For i < k the rows p_i
+// and q_i of every sequence that has not rejected yet (accept[n] == k) are
+// streamed, kRowParts CTAs each; the last CTA merges both rows' statistics,
+// stores them where row_stats would, and tests draft i.  For i == k the bonus
+// row p_k of every sequence that accepted all k drafts is streamed and its
+// chunk statistics kept for the pick.  A sequence is finished at its
+// rejection (or at i == k): accepted drafts, -1 padding and n_accepted are
+// written then.  Sequences that rejected earlier return at once, so no row
+// after a sequence's first rejection is read.
+template <bool VEC>
+__global__ void __launch_bounds__(kStatThreads)
+    seq_step_kernel(const float* __restrict__ p, const float* __restrict__ q,
+                    const int32_t* __restrict__ drafts, int N, int k, int V, int i, uint64_t seed,
+                    uint32_t offset, float2* __restrict__ stats, float2* __restrict__ pchunks,
+                    float2* __restrict__ qchunks, int32_t* accept, int* __restrict__ arrivals,
+                    int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err) {
+  const int rows = i < k ? 2 : 1;
+  const int per_seq = rows * kRowParts;
+  const int n = blockIdx.x / per_seq;
+  const int rem = blockIdx.x - n * per_seq;
+  const int which = rem / kRowParts;      // 0: p_i, 1: q_i
+  const int part = rem - which * kRowParts;
+  if (i > 0 && accept[n] != k) return;    // rejected at an earlier position
+  const float* x = which == 0 ? p + (static_cast<int64_t>(n) * (k + 1) + i) * V
+                              : q + (static_cast<int64_t>(n) * k + i) * V;
+  float2* pc = pchunks + static_cast<int64_t>(n) * kSampleChunks;
+  float2* qc = qchunks + static_cast<int64_t>(n) * kSampleChunks;
+  if (!split_chunks_arrive<VEC>(x, V, part, which == 0 ? pc : qc, arrivals + n, per_seq)) return;
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const float2 rp = merge_chunk_stats(__ldcg(pc + lane));
+  float2 rq = make_float2(0.f, 0.f);
+  if (i < k) rq = merge_chunk_stats(__ldcg(qc + lane));
+  int first = k;
+  if (lane == 0) {
+    arrivals[n] = 0;
+    stats[static_cast<int64_t>(n) * (k + 1) + i] = rp;
+    if (i < k) {
+      stats[static_cast<int64_t>(N) * (k + 1) + static_cast<int64_t>(n) * k + i] = rq;
+      const int x_i = __ldg(drafts + static_cast<int64_t>(n) * k + i);
+      bool rej = true;
+      if (x_i < 0 || x_i >= V) {
+        report_error(err, S3R_DEVERR_BAD_TOKEN);
+      } else {
+        rej = ratio_rejects(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x_i),
+                            __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x_i), rp, rq,
+                            philox_uniform(seed, offset, n, i, kStreamAccept));
+      }
+      first = rej ? i : k;
+      accept[n] = first;
+    }
+  }
+  first = __shfl_sync(0xffffffffu, first, 0);
+  if (i == k || first == i) {
+    int32_t* out = out_tokens + static_cast<int64_t>(n) * (k + 1);
+    for (int j = lane; j <= k; j += 32) {
+      if (j < first) out[j] = __ldg(drafts + static_cast<int64_t>(n) * k + j);
+      else if (j > first) out[j] = -1;
+    }
+    if (lane == 0) n_accepted[n] = first;
+  }
+}
+
+// chunk_sum then pick, after the ratio tests have set accept[] and the stats.
+cudaError_t launch_residual_pick(const float* p, const float* q, int N, int k, int V, uint64_t seed,
+                                 uint32_t offset, const float2* stats, const float2* bonus,
+                                 const int32_t* accept, double2* chunks, int32_t* out_tokens, bool vec,
+                                 cudaStream_t stream) {
+  const unsigned chunk_blocks = static_cast<unsigned>(static_cast<int64_t>(N) * kRowParts);
+  if (vec) {
+    chunk_sum_kernel<true><<<chunk_blocks, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, accept, chunks);
+  } else {
+    chunk_sum_kernel<false><<<chunk_blocks, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, accept, chunks);
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  pick_kernel<<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks,
+                                              out_tokens);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -560,7 +673,8 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
   L.accept_off = L.stats_off + al(static_cast<size_t>(N) * (2 * k + 1) * sizeof(float2));
   L.chunk_off = L.accept_off + al(static_cast<size_t>(N) * sizeof(int32_t));
   L.bonus_off = L.chunk_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(double2));
-  L.total = L.bonus_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(float2));
+  L.arrive_off = L.bonus_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(float2));
+  L.total = L.arrive_off + al(static_cast<size_t>(N) * sizeof(int));
   return L;
 }
 
@@ -576,16 +690,18 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   int32_t* accept = reinterpret_cast<int32_t*>(w + L.accept_off);
   double2* chunks = reinterpret_cast<double2*>(w + L.chunk_off);
   float2* bonus = reinterpret_cast<float2*>(w + L.bonus_off);
+  int* arrivals = reinterpret_cast<int*>(w + L.arrive_off);
   const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
                    (k == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
   if (k == 0) {
     const int pos = u_pos >= 0 ? u_pos : 0;
+    const unsigned blocks = static_cast<unsigned>(static_cast<int64_t>(N) * kRowParts);
     if (vec) {
-      bonus_sample_kernel<true><<<N, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, out_tokens,
-                                                                n_accepted);
+      bonus_sample_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, bonus,
+                                                                     arrivals, out_tokens, n_accepted);
     } else {
-      bonus_sample_kernel<false><<<N, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, out_tokens,
-                                                                 n_accepted);
+      bonus_sample_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, bonus,
+                                                                      arrivals, out_tokens, n_accepted);
     }
     return cudaGetLastError();
   }
@@ -601,24 +717,42 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
                                                   out_tokens, n_accepted, err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t chunk_blocks = static_cast<int64_t>(N) * kSampleChunks;
-  if (vec) {
-    chunk_sum_kernel<true><<<static_cast<unsigned>(chunk_blocks), 256, 0, stream>>>(p, q, N, k, V, stats,
-                                                                                   accept, chunks);
-  } else {
-    chunk_sum_kernel<false><<<static_cast<unsigned>(chunk_blocks), 256, 0, stream>>>(p, q, N, k, V, stats,
-                                                                                    accept, chunks);
+  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, stream);
+}
+
+cudaError_t launch_spec_sample_sequential(const float* p, const float* q, const int32_t* drafts, int N, int k,
+                                          int V, uint64_t seed, uint32_t offset, void* ws,
+                                          int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream) {
+  if (N == 0) return cudaSuccess;
+  if (k == 0) return launch_spec_sample(p, q, drafts, N, k, V, seed, offset, ws, out_tokens, n_accepted, stream);
+  const SpecWorkspaceLayout L = spec_workspace_layout(N, k);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* err = reinterpret_cast<int*>(w + L.err_off);
+  float2* stats = reinterpret_cast<float2*>(w + L.stats_off);
+  int32_t* accept = reinterpret_cast<int32_t*>(w + L.accept_off);
+  double2* chunks = reinterpret_cast<double2*>(w + L.chunk_off);
+  // the draft rows' chunk statistics live in the chunk-sum area until the
+  // residual chunk sums overwrite it after the last step
+  float2* qchunks = reinterpret_cast<float2*>(chunks);
+  float2* bonus = reinterpret_cast<float2*>(w + L.bonus_off);
+  int* arrivals = reinterpret_cast<int*>(w + L.arrive_off);
+  const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(p) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(q) % 16 == 0);
+  for (int i = 0; i <= k; ++i) {
+    const unsigned blocks = static_cast<unsigned>(static_cast<int64_t>(N) * (i < k ? 2 : 1) * kRowParts);
+    if (vec) {
+      seq_step_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, q, drafts, N, k, V, i, seed, offset, stats,
+                                                                 bonus, qchunks, accept, arrivals, out_tokens,
+                                                                 n_accepted, err);
+    } else {
+      seq_step_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, q, drafts, N, k, V, i, seed, offset, stats,
+                                                                  bonus, qchunks, accept, arrivals, out_tokens,
+                                                                  n_accepted, err);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (vec) {
-    pick_kernel<true><<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks,
-                                                      out_tokens);
-  } else {
-    pick_kernel<false><<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks,
-                                                       out_tokens);
-  }
-  return cudaGetLastError();
+  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, stream);
 }
 
 }  // namespace s3r

@@ -17,6 +17,7 @@ struct SpecWorkspaceLayout {
   size_t accept_off;  // int32 [N]: accepted count a = index of the row sampled from
   size_t chunk_off;   // double2 [N][kSampleChunks]: (residual sum, target-row sum) per chunk
   size_t bonus_off;   // float2 [N][kSampleChunks]: (max, sum) per chunk of the bonus row p_k
+  size_t arrive_off;  // int32 [N]: per-sequence arrival counters, zero between calls
   size_t total;
 };
 
@@ -32,5 +33,12 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
                                int V, uint64_t seed, uint32_t offset, void* ws,
                                int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
                                uint32_t u_stream = 1, int u_pos = -1);
+
+// The same sampling with the ratio tests taken one position at a time
+// (k + 1 step launches): a sequence's rows after its first rejection are
+// never read.  Same outputs as launch_spec_sample.
+cudaError_t launch_spec_sample_sequential(const float* p, const float* q, const int32_t* drafts, int N, int k,
+                                          int V, uint64_t seed, uint32_t offset, void* ws,
+                                          int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream);
 
 }  // namespace s3r

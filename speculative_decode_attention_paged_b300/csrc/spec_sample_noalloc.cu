@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "../../include/s3r.h"
+#include "spec_sample.cuh"
 
 #include <cuda_runtime.h>
 
@@ -59,8 +60,15 @@ extern "C" s3r_status s3r_spec_sample_noalloc(const float* p_logits, const float
   void* ws = scratch_address();
   if (ws == nullptr) return S3R_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: clear the error word.
+  // The array keeps the previous call's contents: clear the error word, and
+  // for k = 0 the per-sequence arrival counters that sampler counts on.
   if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return S3R_ERR_CUDA;
+  if (k == 0 && n > 0) {
+    const s3r::SpecWorkspaceLayout L = s3r::spec_workspace_layout(n, k);
+    if (cudaMemsetAsync(static_cast<unsigned char*>(ws) + L.arrive_off, 0, static_cast<size_t>(n) * sizeof(int),
+                        s) != cudaSuccess)
+      return S3R_ERR_CUDA;
+  }
   const s3r_status r = s3r_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed, offset,
                                        out_tokens, n_accepted, ws, S3R_NOALLOC_SCRATCH_BYTES, stream);
   if (r != S3R_OK) return r;

@@ -50,7 +50,8 @@ def _no_alloc_through_c_abi(inp):
 def test_no_alloc_matches_workspace_entry_point_on_two_calls():
     first = make_spec_inputs(512, 8, 151936, 3.0, 1.0, seed=71, device=DEV)
     second = make_spec_inputs(300, 3, 5003, 2.0, 0.5, seed=72, device=DEV)
-    for inp in (first, second):
+    bonus_only = make_spec_inputs(700, 0, 32000, 3.0, 1.0, seed=73, device=DEV)   # k = 0: arrival counters
+    for inp in (first, second, bonus_only, bonus_only):
         ref_out, ref_nacc = _with_workspace(inp)
         out, nacc, err = _no_alloc_through_c_abi(inp)
         assert err == 0
