@@ -729,66 +729,105 @@ def run_sampler(args):
 
 
 def run_layers(args):
-    """Multi-layer draft-verify round: all 28 layers of the Qwen3-1.7B
-    attention geometry, 32 sequences with histories U{4096..16384} in a pool
-    sized for 16K tokens per sequence (~60 GB), per-layer random queries,
-    budget 0.05, k = T = 4.  A round = 4 sparse draft steps over all layers,
-    verify with page mass and selection for every layer (feeding the next
-    round's drafts), captured in one CUDA graph; compared with 4 dense decode
-    steps over all layers (a second graph)."""
+    """Closed multi-layer S³R round: all 28 layers of the Qwen3-1.7B attention
+    geometry, 32 sequences with histories U{4096..16384} in a pool sized for
+    16K tokens per sequence (~60 GB), per-layer random queries and K/V rows,
+    budget 0.05, k = 4, synthetic logits over V = 151936 (p ~ N(0, 3^2),
+    q = p + N(0, 1)).  One round, captured in one CUDA graph:
+      4 draft steps: every layer appends its draft row at L + j and runs sparse
+        draft attention over the previous round's pages; the draft token is
+        sampled from q_j in place;
+      verify: every layer appends the k + 1 dense rows of [pending token,
+        drafts] at L .. L + k and verifies them with page mass;
+      exact speculative sampling of the 32 blocks, the length commit
+        L' = L + n_acc + 1, and every layer's pages for the next round over L'.
+    Compared with 4 dense decode steps (a second graph): every layer appends
+    the step's row and runs dense attention, then a token is sampled from p_j.
+    Both graphs restart from the same L at every replay (the appends rewrite
+    the same slots), so each timed step is the same round."""
     import speculative_decode_attention_paged_b300 as s3r
     dev = torch.device("cuda", torch.cuda.current_device())
     c = ATTN_CONFIGS[5]
+    sc = SAMPLER_CONFIGS[2]
     S, k, Hq, Hkv, n_layers = (args.seqs or c.num_seqs), c.k, c.q_heads, c.kv_heads, c.layers
     if args.layers:
         n_layers = args.layers
+    budget, V = c.budgets[0], sc.vocab
     gen = torch.Generator(device="cpu")
     gen.manual_seed(c.seed)
     L = torch.randint(c.hist_min, c.hist_max + 1, (S,), generator=gen).to(torch.int32)
     if args.all_16k:
         L = torch.full((S,), c.capacity_tokens - 2 * k, dtype=torch.int32)
+    rows_gen = torch.Generator(device=dev)
+    rows_gen.manual_seed(c.seed + 1)
+
+    def bf16_rows(*shape):
+        return (torch.randn(shape, generator=rows_gen, device=dev)).to(torch.bfloat16)
+
     layers = []
     for li in range(n_layers):
         kv = make_paged_kv(S, Hq, Hkv, 2 * k, seed=c.seed * 1000 + li, device=dev, hist_lens=L.to(dev),
                            capacity_tokens=c.capacity_tokens)
         desc = s3r.PagedKVDesc(kv.k_pool, kv.v_pool, kv.block_table, Hq)
-        b_max = selection_budget_pages(kv.max_pages, c.budgets[0])
+        b_max = selection_budget_pages(kv.max_pages, budget)
         layers.append(dict(
             kv=kv, desc=desc,
-            qv=make_queries(kv, 5000 + li, rows=k), qd=[make_queries(kv, 5100 + 16 * li + j) for j in range(k)],
-            out_v=torch.empty((S, k, Hq, 128), dtype=torch.float32, device=dev),
+            qv=make_queries(kv, 5000 + li, rows=k + 1), qd=[make_queries(kv, 5100 + 16 * li + j) for j in range(k)],
+            draft_kv=[(bf16_rows(S, 1, Hkv, 128), bf16_rows(S, 1, Hkv, 128)) for _ in range(k)],
+            block_kv=(bf16_rows(S, k + 1, Hkv, 128), bf16_rows(S, k + 1, Hkv, 128)),
+            out_v=torch.empty((S, k + 1, Hq, 128), dtype=torch.float32, device=dev),
             out_d=[torch.empty((S, Hq, 128), dtype=torch.float32, device=dev) for _ in range(k)],
             mass=torch.empty((S, Hkv, kv.max_pages), dtype=torch.float32, device=dev),
             sel=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
-            cnt=torch.empty((S, Hkv), dtype=torch.int32, device=dev)))
+            cnt=torch.empty((S, Hkv), dtype=torch.int32, device=dev),
+            sel_next=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
+            cnt_next=torch.empty((S, Hkv), dtype=torch.int32, device=dev)))
+    max_len = layers[0]["kv"].max_pages * 16
+    spec = make_spec_inputs(S, k, V, sc.p_sigma, sc.q_sigmas[0], sc.seed, device=dev)
+    drafts = torch.empty((S, k), dtype=torch.int32, device=dev)
+    out_tokens = torch.empty((S, k + 1), dtype=torch.int32, device=dev)
+    n_acc = torch.empty((S,), dtype=torch.int32, device=dev)
+    dense_tokens = torch.empty((S, k), dtype=torch.int32, device=dev)
     Ld = L.to(dev)
-    sel_lens = (Ld + k).to(torch.int32)
+    L_next = torch.empty_like(Ld)
+    starts = [(Ld + j).to(torch.int32) for j in range(k)]
     ctx = [(Ld + j + 1).to(torch.int32) for j in range(k)]
-    ws = s3r.Workspace(s3r.s3r_attn_workspace_size(layers[0]["desc"], k), device=dev)
+    ws = s3r.Workspace(s3r.s3r_attn_workspace_size(layers[0]["desc"], k + 1), device=dev)
+    sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(S, k), device=dev)
+    dws = s3r.Workspace(s3r.s3r_sample_draft_workspace_size(S), device=dev)
     pool_gb = sum(2 * l["kv"].k_pool.numel() * 2 for l in layers) / 1e9
-
-    def verify_select():
-        for l in layers:
-            s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
-            s3r.s3r_select_draft_pages(l["mass"], sel_lens, c.budgets[0], l["sel"], l["cnt"], ws)
 
     def s3r_round():
         for j in range(k):
             for l in layers:
-                s3r.s3r_sparse_draft_attn(l["desc"], sel_lens, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0,
-                                          ws)
-        verify_select()
+                s3r.s3r_kv_append(l["desc"], starts[j], l["draft_kv"][j][0], l["draft_kv"][j][1], ws)
+                s3r.s3r_sparse_draft_attn(l["desc"], Ld, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0, ws)
+            s3r.s3r_sample_draft_tokens(spec.q_logits[:, j], sc.philox_seed, 0, j, drafts[:, j], dws)
+        for l in layers:
+            s3r.s3r_kv_append(l["desc"], Ld, l["block_kv"][0], l["block_kv"][1], ws)
+            s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
+        s3r.s3r_spec_sample(spec.p_logits, spec.q_logits, drafts, sc.philox_seed, 0, out_tokens, n_acc, sws)
+        s3r.s3r_commit_lengths(Ld, n_acc, k, max_len, L_next, ws)
+        for l in layers:
+            s3r.s3r_select_draft_pages(l["mass"], L_next, budget, l["sel_next"], l["cnt_next"], ws)
 
     def dense_steps():
         for j in range(k):
             for l in layers:
+                s3r.s3r_kv_append(l["desc"], starts[j], l["draft_kv"][j][0], l["draft_kv"][j][1], ws)
                 s3r.s3r_dense_decode_attn(l["desc"], ctx[j], l["qd"][j], l["out_d"][j], 1.0, ws)
+            s3r.s3r_sample_draft_tokens(spec.p_logits[:, j], sc.philox_seed, 0, j, dense_tokens[:, j], dws)
 
-    verify_select()           # selections for the first round's drafts
+    # the first round's pages: a verify of the block at L, selected over L + k (a previous round)
+    for l in layers:
+        s3r.s3r_kv_append(l["desc"], Ld, l["block_kv"][0], l["block_kv"][1], ws)
+        s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
+        s3r.s3r_select_draft_pages(l["mass"], (Ld + k).to(torch.int32), budget, l["sel"], l["cnt"], ws)
     s3r_round()
     dense_steps()
     torch.cuda.synchronize()
-    ws.check()
+    for w in (ws, sws, dws):
+        w.check()
     # CUDA graphs: one per round, one per 4 dense steps (the calls enqueue on torch's current stream)
     g_round, g_dense = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
@@ -805,27 +844,38 @@ def run_layers(args):
     t_dense = _timed(g_dense.replay, args.steps, args.warmup)
     t_round_eager = _timed(s3r_round, max(2, args.steps // 4), 1)
     clock_info = clocks.stop()
-    ws.check()
+    for w in (ws, sws, dws):
+        w.check()
+    a = n_acc.cpu().numpy().astype(np.int64)
+    if not np.array_equal(L_next.cpu().numpy(), L.numpy() + a + 1):
+        raise RuntimeError("length commit differs from L + n_acc + 1")
     Lsum = float(L.double().sum())
-    tok = [sum(_visible_draft_tokens(l["sel"], l["cnt"], sel_lens, j) for l in layers) for j in range(k)]
+    tok = [sum(_visible_draft_tokens(l["sel"], l["cnt"], Ld, j) for l in layers) for j in range(k)]
+    row_bytes = Hkv * KV_TOKEN_BYTES_PER_HEAD                       # K + V of one token, all KV heads
     draft_bytes = sum(t * KV_TOKEN_BYTES_PER_HEAD for t in tok) + k * n_layers * S * Hq * 128 * 6
-    verify_bytes = n_layers * ((Lsum + S * k) * Hkv * KV_TOKEN_BYTES_PER_HEAD + S * k * Hq * 128 * 6
+    verify_bytes = n_layers * ((Lsum + S * (k + 1)) * row_bytes + S * (k + 1) * Hq * 128 * 6
                                + 2 * S * Hkv * layers[0]["kv"].max_pages * 4)
-    dense_bytes = n_layers * sum((Lsum + S * (j + 1)) * Hkv * KV_TOKEN_BYTES_PER_HEAD + S * Hq * 128 * 6
-                                 for j in range(k))
-    round_bytes = draft_bytes + verify_bytes
+    append_bytes = n_layers * 2 * S * (2 * k + 1) * row_bytes       # rows read and written
+    sample_bytes = S * k * V * 4 + S * (2 * k + 1) * V * 4
+    dense_bytes = n_layers * sum((Lsum + S * (j + 1)) * row_bytes + S * Hq * 128 * 6 for j in range(k)) \
+        + n_layers * 2 * S * k * row_bytes + S * k * V * 4
+    round_bytes = draft_bytes + verify_bytes + append_bytes + sample_bytes
+    emitted = float((a + 1).sum())
     return {"workload": f"qwen3-1.7b-geom {n_layers} layers: {S} seqs x "
                         + ("all 16K" if args.all_16k else "U{4096..16384}") + f" in a {pool_gb:.1f} GB pool, "
-                        f"budget 0.05, k=T=4, one CUDA graph per round",
+                        f"budget {budget}, k={k}, verify k+1 rows, V={V} (sigma {sc.q_sigmas[0]}); "
+                        "closed round in one CUDA graph",
             "metric": METRIC, "value": round_bytes / (t_round * 1e-3) / 1e9, "unit": UNIT,
             "round_ms": t_round, "round_ms_eager": t_round_eager, "round_gb": round_bytes / 1e9,
             "dense_4_steps_ms": t_dense, "dense_gb": dense_bytes / 1e9,
             "dense_gbs": dense_bytes / (t_dense * 1e-3) / 1e9,
-            "speedup_vs_dense": t_dense / t_round,
-            "draft_verify_tokens_per_s": S * k / (t_round * 1e-3),
-            "dense_tokens_per_s": S * k / (t_dense * 1e-3),
-            "launches_per_round": n_layers * (2 * k + 2), "clocks": clock_info}
-
+            "round_vs_4_dense_time": t_dense / t_round,
+            "mean_accepted": float(a.mean()), "mean_emitted_per_round": emitted / S,
+            "s3r_emitted_tokens_per_s": emitted / (t_round * 1e-3),
+            "dense_emitted_tokens_per_s": S * k / (t_dense * 1e-3),
+            "emitted_tokens_speedup": (emitted / t_round) / (S * k / t_dense),
+            "launches_per_round": n_layers * (2 * k + 3) + k + 4 + 1,
+            "launches_per_dense_4_steps": k * (2 * n_layers + 1), "clocks": clock_info}
 
 
 def main(argv=None):

@@ -263,16 +263,63 @@ S3R_API s3r_status s3r_sample_draft_workspace_size(int32_t n, size_t* bytes);
  * rebasdaily.com, "草稿可以稀疏，交卷必须完整"), here at draft step
  * `draft_pos` of every sequence.
  *
- *   logits  fp32 [n][vocab], the drafter's logits at this step
- *   tokens  int32 [n] out
+ *   logits        fp32, row s (vocab values) at logits + s * row_stride; the
+ *                 drafter's logits at this step.  row_stride >= vocab
+ *                 (elements), so the rows may be one slice [n][j][vocab] of
+ *                 a [n][k][vocab] block of draft logits (row_stride = k*vocab)
+ *   tokens        int32 out: token s at tokens[s * token_stride]
+ *                 (token_stride >= 1, e.g. k for column j of [n][k] drafts)
  * token[s] is the inverse CDF, in token-id order, of softmax(logits[s])
  * (temperature 1) at the Philox4x32-10 uniform of counter
  * (s, draft_pos, 2, offset) and key seed (stream 2 = DRAFT), with the same
  * uniform and inverse-CDF conventions as s3r_spec_sample.  offset < 2^32.
+ * Its workspace must hold zeroed arrival counters (s3r_workspace_init once);
+ * every call leaves them at zero.
  */
-S3R_API s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, uint64_t seed,
-                                   uint64_t offset, int32_t draft_pos, int32_t* tokens, void* ws,
-                                   size_t ws_bytes, void* stream);
+S3R_API s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, int64_t row_stride,
+                                   uint64_t seed, uint64_t offset, int32_t draft_pos, int32_t* tokens,
+                                   int64_t token_stride, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Append a block of K/V rows to every sequence's paged cache.  The drafter
+ * writes the row of each draft step, and verification the dense rows of the
+ * verified block, which the system keeps for the accepted part (wispaper.ai,
+ * "S3R drafts sparsely and verifies densely"; rit.work, "Как разреженный
+ * черновик сохраняет ответы плотной модели").
+ *
+ *   kv          the layer's cache; its k_pool and v_pool are WRITTEN (they
+ *               are const in s3r_paged_kv because attention only reads them)
+ *   start_lens  int32 [num_seqs]: position of row 0 (the length L before it)
+ *   n_rows      int32 [num_seqs] rows to write per sequence, in [0, max_rows];
+ *               NULL writes max_rows rows for every sequence
+ *   k_rows, v_rows  bf16 [num_seqs][max_rows][num_kv_heads][128], 16-byte
+ *               aligned; row t of sequence s goes to position L + t: slot
+ *               (L + t) % 16 of page block_table[s][(L + t) / 16]
+ * Rows beyond the block table set S3R_DEVERR_BAD_LENGTH, page ids outside the
+ * pool S3R_DEVERR_BAD_PAGE, and a count outside [0, max_rows]
+ * S3R_DEVERR_BAD_COUNT; such rows are not written.  ws: any workspace of at
+ * least 256 bytes (its error word is used).
+ */
+S3R_API s3r_status s3r_kv_append(const s3r_paged_kv* kv, const int32_t* start_lens, const int32_t* n_rows,
+                                 int32_t max_rows, const void* k_rows, const void* v_rows, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/*
+ * Commit a verified block: new_lens[s] = hist_lens[s] + n_accepted[s] + 1,
+ * the pending token and the accepted drafts, whose dense rows the block's
+ * s3r_kv_append wrote at positions L .. L + n_accepted.  The rejected drafts'
+ * rows lie past the new length: they are dropped (rolled back) and the next
+ * round's appends overwrite them (rebasdaily.com and rit.work: a rejected
+ * draft and everything after it is discarded).
+ *
+ *   hist_lens, n_accepted  int32 [n]; new_lens int32 [n] out (may be hist_lens)
+ * n_accepted outside [0, max_accept] sets S3R_DEVERR_BAD_COUNT and a new length
+ * above max_len S3R_DEVERR_BAD_LENGTH; such a sequence keeps its length.
+ * ws: any workspace of at least 256 bytes.
+ */
+S3R_API s3r_status s3r_commit_lengths(const int32_t* hist_lens, const int32_t* n_accepted, int32_t n,
+                                      int32_t max_accept, int32_t max_len, int32_t* new_lens, void* ws,
+                                      size_t ws_bytes, void* stream);
 
 /* Bytes of library-owned device scratch behind s3r_spec_sample_noalloc, held
  * once by every GPU that loads the library until the process exits. */

@@ -34,6 +34,8 @@ from .selection import select_draft_pages, selection_budget
 from .philox import philox4x32_10, philox_uniform, STREAM_ACCEPT, STREAM_RESAMPLE, STREAM_DRAFT
 from .spec_sample import spec_sample, residual_row
 from .draft_sample import sample_draft_tokens
+from .kv_cache import kv_append, commit_lengths
+from .round import closed_round
 
 __all__ = [
     "PAGE_SIZE",
@@ -51,4 +53,7 @@ __all__ = [
     "spec_sample",
     "residual_row",
     "sample_draft_tokens",
+    "kv_append",
+    "commit_lengths",
+    "closed_round",
 ]

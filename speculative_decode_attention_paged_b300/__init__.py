@@ -33,6 +33,8 @@ __all__ = [
     "s3r_spec_sample_noalloc",
     "s3r_sample_draft_workspace_size",
     "s3r_sample_draft_tokens",
+    "s3r_kv_append",
+    "s3r_commit_lengths",
     "DEVERR_BAD_PAGE",
     "DEVERR_BAD_LENGTH",
     "DEVERR_BAD_TOKEN",
@@ -106,8 +108,10 @@ _SIG = {
     "s3r_spec_sample_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
                                                _P, _P, _P, _P]),
     "s3r_sample_draft_workspace_size": (ctypes.c_int, [_I32, ctypes.POINTER(ctypes.c_size_t)]),
-    "s3r_sample_draft_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64, _I32, _P, _P,
-                                               ctypes.c_size_t, _P]),
+    "s3r_sample_draft_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
+                                               _I32, _P, ctypes.c_int64, _P, ctypes.c_size_t, _P]),
+    "s3r_kv_append": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _P, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
+    "s3r_commit_lengths": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -348,11 +352,55 @@ def s3r_sample_draft_workspace_size(n):
     return out.value
 
 
+def _need_rows(t, dtype, name, dims):
+    """A CUDA tensor of `dims` dimensions whose last dimension is contiguous
+    (rows may be strided, e.g. one slice of a larger block)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != dims or (dims > 1 and t.stride(-1) != 1):
+        raise ValueError(f"{name} must be {dims}-D with a contiguous last dimension")
+    return t
+
+
 def s3r_sample_draft_tokens(logits, seed, offset, draft_pos, tokens, ws: Workspace, stream=None):
-    """One draft token per sequence from softmax(logits) [n][vocab] (fp32)."""
-    _need(logits, torch.float32, "logits")
-    _need(tokens, torch.int32, "tokens")
+    """One draft token per sequence from softmax(logits[s]) (fp32 [n][vocab],
+    rows may be strided, e.g. q_logits[:, j]); token s goes to tokens[s]
+    (int32 [n], may be strided, e.g. drafts[:, j])."""
+    _need_rows(logits, torch.float32, "logits", 2)
+    _need_rows(tokens, torch.int32, "tokens", 1)
     n, V = logits.shape
-    _call("s3r_sample_draft_tokens", _ptr(logits), _I32(n), _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset),
-          _I32(draft_pos), _ptr(tokens), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    if tokens.shape[0] != n:
+        raise ValueError("tokens must have one entry per logits row")
+    _call("s3r_sample_draft_tokens", _ptr(logits), _I32(n), _I32(V), ctypes.c_int64(logits.stride(0) if n > 1 else V),
+          ctypes.c_uint64(seed), ctypes.c_uint64(offset), _I32(draft_pos), _ptr(tokens),
+          ctypes.c_int64(tokens.stride(0) if n > 1 else 1), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
     return tokens
+
+
+def s3r_kv_append(kv: PagedKVDesc, start_lens, k_rows, v_rows, ws: Workspace, n_rows=None, stream=None):
+    """Write k_rows / v_rows (bf16 [S][max_rows][Hkv][128]) at positions
+    start_lens[s] + t of each sequence's pages; n_rows (int32 [S]) limits the
+    rows per sequence (default: all).  The descriptor's pools are written."""
+    _need(start_lens, torch.int32, "start_lens")
+    _need(k_rows, torch.bfloat16, "k_rows")
+    _need(v_rows, torch.bfloat16, "v_rows")
+    if k_rows.shape != v_rows.shape or k_rows.dim() != 4 or k_rows.shape[0] != kv.num_seqs:
+        raise ValueError("k_rows and v_rows must both be [num_seqs][max_rows][num_kv_heads][head_dim]")
+    if n_rows is not None:
+        _need(n_rows, torch.int32, "n_rows")
+    _call("s3r_kv_append", ctypes.byref(kv.c), _ptr(start_lens), _ptr(n_rows) if n_rows is not None else None,
+          _I32(k_rows.shape[1]), _ptr(k_rows), _ptr(v_rows), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+
+
+def s3r_commit_lengths(hist_lens, n_accepted, max_accept, max_len, new_lens, ws: Workspace, stream=None):
+    """new_lens = hist_lens + n_accepted + 1 (new_lens may be hist_lens)."""
+    _need(hist_lens, torch.int32, "hist_lens")
+    _need(n_accepted, torch.int32, "n_accepted")
+    _need(new_lens, torch.int32, "new_lens")
+    _call("s3r_commit_lengths", _ptr(hist_lens), _ptr(n_accepted), _I32(hist_lens.shape[0]), _I32(max_accept),
+          _I32(max_len), _ptr(new_lens), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    return new_lens

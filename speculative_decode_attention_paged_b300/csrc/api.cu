@@ -10,6 +10,7 @@
 #include "attn_paged.cuh"
 #include "s3r_device.cuh"
 #include "spec_sample.cuh"
+#include "kv_append.cuh"
 
 namespace s3r {
 cudaError_t launch_select_pages(const float* mass, const int32_t* sel_lens, int S, int Hkv,
@@ -361,12 +362,12 @@ s3r_status s3r_spec_sample_sequential(const float* p_logits, const float* q_logi
                                                  static_cast<cudaStream_t>(stream)));
 }
 
-s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, uint64_t seed,
-                                   uint64_t offset, int32_t draft_pos, int32_t* tokens, void* ws,
-                                   size_t ws_bytes, void* stream) {
-  if (n < 0 || vocab <= 0 || draft_pos < 0) return S3R_ERR_INVALID_ARG;
+s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, int64_t row_stride,
+                                   uint64_t seed, uint64_t offset, int32_t draft_pos, int32_t* tokens,
+                                   int64_t token_stride, void* ws, size_t ws_bytes, void* stream) {
+  if (n < 0 || vocab <= 0 || draft_pos < 0 || row_stride < vocab || token_stride < 1) return S3R_ERR_INVALID_ARG;
   if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(n) * vocab > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(n) * row_stride > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(n) * kSampleChunks > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
   size_t need = 0;
   s3r_sample_draft_workspace_size(n, &need);
@@ -377,13 +378,52 @@ s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab
   int32_t* count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.accept_off);
   return to_status(launch_spec_sample(logits, nullptr, nullptr, n, 0, vocab, seed, static_cast<uint32_t>(offset),
                                       ws, tokens, count, static_cast<cudaStream_t>(stream), kStreamDraftU,
-                                      draft_pos));
+                                      draft_pos, row_stride, token_stride));
 }
 
 s3r_status s3r_sample_draft_workspace_size(int32_t n, size_t* bytes) {
   if (bytes == nullptr || n < 0) return S3R_ERR_INVALID_ARG;
   *bytes = spec_workspace_layout(n, 0).total;
   return S3R_OK;
+}
+
+s3r_status s3r_kv_append(const s3r_paged_kv* kv, const int32_t* start_lens, const int32_t* n_rows,
+                         int32_t max_rows, const void* k_rows, const void* v_rows, void* ws, size_t ws_bytes,
+                         void* stream) {
+  const s3r_status st = validate_kv(kv);
+  if (st != S3R_OK) return st;
+  if (max_rows < 0) return S3R_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return S3R_ERR_WORKSPACE;
+  if (static_cast<int64_t>(kv->num_seqs) * max_rows > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
+  if (kv->num_seqs == 0 || max_rows == 0) return S3R_OK;
+  if (start_lens == nullptr || k_rows == nullptr || v_rows == nullptr) return S3R_ERR_INVALID_ARG;
+  if (!aligned16(k_rows) || !aligned16(v_rows)) return S3R_ERR_INVALID_ARG;
+  KvAppendArgs a{};
+  // the pools are declared const in s3r_paged_kv because attention only reads them
+  a.k_pool = const_cast<void*>(kv->k_pool);
+  a.v_pool = const_cast<void*>(kv->v_pool);
+  a.block_table = kv->block_table;
+  a.num_phys_pages = kv->num_phys_pages;
+  a.max_pages = kv->max_pages_per_seq;
+  a.S = kv->num_seqs;
+  a.Hkv = kv->num_kv_heads;
+  a.start_lens = start_lens;
+  a.n_rows = n_rows;
+  a.max_rows = max_rows;
+  a.k_rows = k_rows;
+  a.v_rows = v_rows;
+  a.err = static_cast<int*>(ws);
+  return to_status(launch_kv_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+s3r_status s3r_commit_lengths(const int32_t* hist_lens, const int32_t* n_accepted, int32_t n, int32_t max_accept,
+                              int32_t max_len, int32_t* new_lens, void* ws, size_t ws_bytes, void* stream) {
+  if (n < 0 || max_accept < 0 || max_len < 0) return S3R_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned256(ws) || ws_bytes < 256) return S3R_ERR_WORKSPACE;
+  if (n == 0) return S3R_OK;
+  if (hist_lens == nullptr || n_accepted == nullptr || new_lens == nullptr) return S3R_ERR_INVALID_ARG;
+  return to_status(launch_commit_lengths(hist_lens, n_accepted, n, max_accept, max_len, new_lens,
+                                         static_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

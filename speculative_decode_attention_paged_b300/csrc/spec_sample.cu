@@ -532,15 +532,17 @@ __device__ __forceinline__ bool split_chunks_arrive(const float* __restrict__ x,
   return last;
 }
 
-// k = 0: one token per sequence from softmax(p_n), kRowParts CTAs per row;
+// k = 0: one token per sequence from softmax(p_n) (row n at p + n * row_stride,
+// token n at out_tokens[n * token_stride]), kRowParts CTAs per row;
 // the last to arrive takes the chunk holding u * Z from the merged chunk
 // statistics and scans it.  The uniform is the one of counter
 // (n, u_pos, u_stream, offset).  Writes n_accepted[n] = 0.
 template <bool VEC>
 __global__ void __launch_bounds__(kStatThreads)
-    bonus_sample_kernel(const float* __restrict__ p, int V, uint64_t seed, uint32_t offset,
+    bonus_sample_kernel(const float* __restrict__ p, int V, int64_t row_stride, uint64_t seed, uint32_t offset,
                         uint32_t u_stream, int u_pos, float2* __restrict__ chunks, int* __restrict__ arrivals,
-                        int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted) {
+                        int32_t* __restrict__ out_tokens, int64_t token_stride,
+                        int32_t* __restrict__ n_accepted) {
   __shared__ PickSmem sm;
   __shared__ float2 s_row;
   __shared__ int s_chunk;
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(kStatThreads)
   const int n = blockIdx.x / kRowParts;
   const int part = blockIdx.x - n * kRowParts;
   const int tid = threadIdx.x;
-  const float* x = p + static_cast<int64_t>(n) * V;
+  const float* x = p + static_cast<int64_t>(n) * row_stride;
   float2* cs_n = chunks + static_cast<int64_t>(n) * kSampleChunks;
   if (!split_chunks_arrive<VEC>(x, V, part, cs_n, arrivals + n, kRowParts)) return;
   if (tid < 32) {
@@ -579,7 +581,7 @@ __global__ void __launch_bounds__(kStatThreads)
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
   const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, sm);
-  if (tid == 0) out_tokens[n] = tok;
+  if (tid == 0) out_tokens[static_cast<int64_t>(n) * token_stride] = tok;
 }
 
 // Step i of the sequential (early-exit) ratio tests.  For i < k the rows p_i
@@ -681,7 +683,7 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                int V, uint64_t seed, uint32_t offset, void* ws,
                                int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
-                               uint32_t u_stream, int u_pos) {
+                               uint32_t u_stream, int u_pos, int64_t row_stride, int64_t token_stride) {
   if (N == 0) return cudaSuccess;
   const SpecWorkspaceLayout L = spec_workspace_layout(N, k);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -695,13 +697,17 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
                    (k == 0 || reinterpret_cast<uintptr_t>(q) % 16 == 0);
   if (k == 0) {
     const int pos = u_pos >= 0 ? u_pos : 0;
+    const int64_t stride = row_stride > 0 ? row_stride : V;
+    const bool vec0 = vec && stride % 4 == 0;
     const unsigned blocks = static_cast<unsigned>(static_cast<int64_t>(N) * kRowParts);
-    if (vec) {
-      bonus_sample_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, bonus,
-                                                                     arrivals, out_tokens, n_accepted);
+    if (vec0) {
+      bonus_sample_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, V, stride, seed, offset, u_stream, pos,
+                                                                     bonus, arrivals, out_tokens, token_stride,
+                                                                     n_accepted);
     } else {
-      bonus_sample_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, V, seed, offset, u_stream, pos, bonus,
-                                                                      arrivals, out_tokens, n_accepted);
+      bonus_sample_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, V, stride, seed, offset, u_stream, pos,
+                                                                      bonus, arrivals, out_tokens, token_stride,
+                                                                      n_accepted);
     }
     return cudaGetLastError();
   }

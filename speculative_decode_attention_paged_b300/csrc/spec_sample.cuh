@@ -28,11 +28,13 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k);
 // Philox uniform of counter (n, a, RESAMPLE, offset), a the accepted count.
 // With k = 0 (no draft rows) one token is sampled from softmax(p) per sequence
 // with the uniform of counter (n, u_pos, u_stream, offset), u_pos < 0 meaning
-// 0, and n_accepted is set to 0.
+// 0, and n_accepted is set to 0; then row n is read at p + n * row_stride
+// (0: V) and its token written to out_tokens[n * token_stride].
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                int V, uint64_t seed, uint32_t offset, void* ws,
                                int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
-                               uint32_t u_stream = 1, int u_pos = -1);
+                               uint32_t u_stream = 1, int u_pos = -1, int64_t row_stride = 0,
+                               int64_t token_stride = 1);
 
 // The same sampling with the ratio tests taken one position at a time
 // (k + 1 step launches): a sequence's rows after its first rejection are

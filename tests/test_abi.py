@@ -79,3 +79,22 @@ def test_argument_validation_on_host(lib):
     assert lib.s3r_spec_sample(None, None, None, 1, 65, 10, 0, 0, None, None, None, 0, None) == 2
     assert lib.s3r_spec_sample(None, None, None, 1, 4, 0, 0, 0, None, None, None, 0, None) == 1
     assert lib.s3r_spec_sample(None, None, None, 1, 4, 10, 0, 1 << 32, None, None, None, 0, None) == 1
+
+
+def test_new_entry_points_validate_on_host(lib):
+    kv = _kv()
+    # the sequential sampler shares the parallel sampler's checks
+    assert lib.s3r_spec_sample_sequential(None, None, None, 1, 65, 10, 0, 0, None, None, None, 0, None) == 2
+    assert lib.s3r_spec_sample_sequential(None, None, None, -1, 4, 10, 0, 0, None, None, None, 0, None) == 1
+    # draft sampling: rows closer than the vocabulary, token stride 0, missing workspace
+    assert lib.s3r_sample_draft_tokens(None, 4, 100, 99, 0, 0, 0, None, 1, None, 0, None) == 1
+    assert lib.s3r_sample_draft_tokens(None, 4, 100, 100, 0, 0, 0, None, 0, None, 0, None) == 1
+    assert lib.s3r_sample_draft_tokens(None, 4, 100, 100, 0, 0, 0, None, 1, None, 0, None) == 4
+    # KV append: no descriptor, negative rows, unsupported head_dim, missing workspace
+    assert lib.s3r_kv_append(None, None, None, 1, None, None, None, 0, None) == 1
+    assert lib.s3r_kv_append(ctypes.byref(kv), None, None, -1, None, None, None, 0, None) == 1
+    assert lib.s3r_kv_append(ctypes.byref(_kv(head_dim=64)), None, None, 1, None, None, None, 0, None) == 2
+    assert lib.s3r_kv_append(ctypes.byref(kv), None, None, 1, None, None, None, 0, None) == 4
+    # length commit: negative sizes, missing workspace
+    assert lib.s3r_commit_lengths(None, None, -1, 4, 100, None, None, 0, None) == 1
+    assert lib.s3r_commit_lengths(None, None, 4, 4, 100, None, None, 0, None) == 4

@@ -12,11 +12,13 @@ import pytest
 
 import oracle.attention as oatt
 import oracle.draft_sample as odraft
+import oracle.kv_cache as okv
 import oracle.philox as ophil
 import oracle.selection as osel
 import oracle.spec_sample  # noqa: F401  (the package re-exports a function of the same name)
 import test_oracle_attention as pins_att
 import test_oracle_draft_sample as pins_draft
+import test_oracle_kv_cache as pins_kv
 import test_oracle_philox as pins_phil
 import test_oracle_select as pins_sel
 import test_oracle_spec_sample as pins_spec
@@ -121,3 +123,17 @@ def test_draft_sampler_on_the_wrong_stream_is_caught(monkeypatch):
     mutant = _mutant(odraft, "sample_draft_tokens", "int(draft_pos), STREAM_DRAFT)", "int(draft_pos), 1)")
     monkeypatch.setattr(pins_draft, "sample_draft_tokens", mutant)
     _fails(pins_draft.test_uniform_logits_give_floor_u_times_v)
+
+
+def test_append_into_the_next_slot_is_caught(monkeypatch):
+    mutant = _mutant(okv, "kv_append", "k_out[page, :, pos % PAGE_SIZE, :] = k_rows[s, t]",
+                     "k_out[page, :, (pos + 1) % PAGE_SIZE, :] = k_rows[s, t]")
+    monkeypatch.setattr(pins_kv, "kv_append", mutant)
+    _fails(pins_kv.test_append_reads_back_through_whole_page_rebuild)
+
+
+def test_commit_without_the_pending_token_is_caught(monkeypatch):
+    mutant = _mutant(okv, "commit_lengths", "np.asarray(n_accepted, dtype=np.int64) + 1",
+                     "np.asarray(n_accepted, dtype=np.int64)")
+    monkeypatch.setattr(pins_kv, "commit_lengths", mutant)
+    _fails(pins_kv.test_commit_closed_form)
