@@ -39,7 +39,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import ATTN_CONFIGS, SAMPLER_CONFIGS, make_paged_kv, make_queries, make_spec_inputs  # noqa: E402
+from workloads import (ATTN_CONFIGS, SAMPLER_CONFIGS, make_paged_kv, make_queries, make_rollout_requests,  # noqa: E402
+                       make_spec_inputs)
 
 METRIC = "KV GB/s (% of 8 TB/s) and draft+verify attention tokens/s at 1 B300"
 UNIT = "GB/s"
@@ -878,6 +879,100 @@ def run_layers(args):
             "launches_per_dense_4_steps": k * (2 * n_layers + 1), "clocks": clock_info}
 
 
+def _host_link_gbs():
+    """Host-to-device copy rate of pinned memory (1 GiB, median of 5), or None
+    without a GPU."""
+    if not torch.cuda.is_available():
+        return None
+    n = 1 << 30
+    src = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    times = []
+    for _ in range(6):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return n / (float(np.median(times[1:])) * 1e-3) / 1e9
+
+
+def run_scheduler(args):
+    """KV-aware AIMD scheduler against offload with a fixed limit of 256 and
+    recompute, simulated by the library's host scheduler over a KV page pool:
+    256 prompts x 8 responses, prompts U{512..2048}, responses log-uniform on
+    [512, 16384], k = 4 with per-position acceptance 0.8; Qwen3-8B KV geometry
+    (36 layers x 8 KV heads x 128, bf16: 2.36 MB per 16-token page) in 100 GB
+    of HBM.  Reported per policy: pages moved per 1000 generated tokens,
+    cumulative moved and recomputed pages, rounds, mean concurrency; and a
+    modelled generation rate: per round k + 1 passes over the 16.4 GB of bf16
+    weights and attention reads of (1 + k * budget) x the running contexts,
+    both at the measured HBM copy rate; moved pages at the measured host-link
+    rate; recomputed pages at a prefill cost of 2 x 8e9 x 16 FLOP each at the
+    measured sustained bf16 rate.  The AIMD constants (not printed by the
+    pages) are those that maximised this modelled rate over a small grid."""
+    from speculative_decode_attention_paged_b300 import scheduler as sched
+    w = make_rollout_requests(256, 8, seed=17, prompt_lo=512, prompt_hi=2048, response_lo=512,
+                              response_hi=16384, k=4, alpha=0.8)
+    page_tokens, k, budget = 16, 4, 0.05
+    kv_token_bytes = 36 * 8 * 128 * 2 * 2
+    weight_bytes = 16.4e9
+    page_bytes = kv_token_bytes * page_tokens
+    pool = int(100e9 // page_bytes)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        peaks = {}
+    hbm = float(peaks.get("hbm_gbs", 6400.0)) * 1e9
+    tflops = float(peaks.get("bf16_tflops_sustained", 1400.0)) * 1e12
+    link = _host_link_gbs()
+    link_src = "measured" if link is not None else "assumed"
+    link = (link or 55.0) * 1e9
+    t_page_move = page_bytes / link
+    t_page_recompute = 2 * 8e9 * page_tokens / tflops
+    common = dict(pool_pages=pool, page_size=page_tokens, block_tokens=k + 1)
+    policies = {
+        "aimd": dict(policy=sched.AIMD, limit_init=64, limit_min=16, limit_max=1024, add_step=4, mult=0.5,
+                     util_low=0.8, util_high=0.98, backlog_max=64),
+        "offload_fixed_256": dict(policy=sched.FIXED_OFFLOAD, limit_init=256, limit_min=256, limit_max=256,
+                                  add_step=0, mult=1.0, util_low=0.0, util_high=1.0, backlog_max=0),
+        "recompute_fixed_256": dict(policy=sched.RECOMPUTE, limit_init=256, limit_min=256, limit_max=256,
+                                    add_step=0, mult=1.0, util_low=0.0, util_high=1.0, backlog_max=0),
+    }
+    res = {}
+    for name, pol in policies.items():
+        cfg = dict(common, **pol)
+        t0 = time.perf_counter()
+        tot, trace = sched.run(cfg, w.prompt_lens, w.response_lens, w.emits, max_steps=200_000)
+        sim_s = time.perf_counter() - t0
+        attn_s = sum(t["ctx_tokens"] for t in trace) * kv_token_bytes * (1 + k * budget) / hbm
+        weights_s = tot["steps"] * (k + 1) * weight_bytes / hbm
+        move_s = (tot["offloaded"] + tot["restored"]) * t_page_move
+        recompute_s = tot["recomputed"] * t_page_recompute
+        model_s = attn_s + weights_s + move_s + recompute_s
+        res[name] = {"rounds": tot["steps"], "tokens": tot["tokens"], "stalled": tot["stalled"],
+                     "pages_moved": tot["offloaded"] + tot["restored"],
+                     "pages_moved_per_1000_tokens": 1000.0 * (tot["offloaded"] + tot["restored"]) / tot["tokens"],
+                     "pages_recomputed": tot["recomputed"],
+                     "moved_plus_recomputed_pages": tot["offloaded"] + tot["restored"] + tot["recomputed"],
+                     "preemptions": tot["preemptions"], "mean_concurrency": tot["running_sum"] / tot["steps"],
+                     "peak_pages": tot["peak_used"], "final_limit": tot["limit_final"],
+                     "model_s": model_s, "model_attention_s": attn_s, "model_weights_s": weights_s,
+                     "model_transfer_s": move_s,
+                     "model_recompute_s": recompute_s, "model_tokens_per_s": tot["tokens"] / model_s,
+                     "simulation_s": sim_s}
+    return {"workload": "AIMD KV scheduler simulation: 2048 rollout requests, Qwen3-8B KV geometry, "
+                        f"{pool} pages of 16 tokens (100 GB)",
+            "metric": "KV cache pages moved per 1000 generated tokens", "value":
+                res["aimd"]["pages_moved_per_1000_tokens"], "unit": "pages/1000 tokens",
+            "higher_is_better": False, "policies": res,
+            "model": {"hbm_gbs": hbm / 1e9, "host_link_gbs": link / 1e9, "host_link": link_src,
+                      "bf16_tflops": tflops / 1e12, "page_bytes": page_bytes, "weight_bytes": weight_bytes,
+                      "draft_budget": budget, "k": k}}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -886,9 +981,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("s3r", "reference"), default="s3r")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("round", "sweep", "sampler", "layers"), default="round",
+    ap.add_argument("--workload", choices=("round", "sweep", "sampler", "layers", "scheduler"), default="round",
                     help="round (default): the 256-sequence S3R round + dense baseline; sweep: Qwen3-8B "
-                         "geometry budget sweep; sampler: 2048 x k=8 sampler; layers: the 28-layer round")
+                         "geometry budget sweep; sampler: 2048 x k=8 sampler; layers: the 28-layer closed round; "
+                         "scheduler: the AIMD KV scheduler simulation (host)")
     ap.add_argument("--layers", type=int, default=None, help="fewer layers for --workload layers")
     ap.add_argument("--all-16k", action="store_true", help="--workload layers with every history at 16K")
     ap.add_argument("--seqs", type=int, default=None,
@@ -903,7 +999,8 @@ def main(argv=None):
         if args.workload != "round":
             import speculative_decode_attention_paged_b300 as s3r
             s3r.load_library()
-            leg = {"sweep": run_sweep, "sampler": run_sampler, "layers": run_layers}[args.workload]
+            leg = {"sweep": run_sweep, "sampler": run_sampler, "layers": run_layers,
+                   "scheduler": run_scheduler}[args.workload]
             line = leg(args)
             line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
                          "data": "synthetic", "l2": "inputs larger than L2"})

@@ -2,7 +2,7 @@
 
     python -m speculative_decode_attention_paged_b300.build [--force]
 
-Compiles every csrc/*.cu with nvcc and links them into
+Compiles every csrc/*.cu (and the host-only csrc/*.cpp) with nvcc and links them into
 speculative_decode_attention_paged_b300/libs3r.so (CUDA runtime linked
 statically; the driver API is reached through the runtime's entry-point query,
 so no libcuda link is needed at build time).  Rebuilds only when a source,
@@ -37,14 +37,15 @@ def _nvcc():
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _digest():
     h = hashlib.sha256()
-    files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
+    files = (_sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")))
+             + sorted(glob.glob(os.path.join(INCLUDE, "*.h"))))
     for f in files:
-        h.update(f.encode())
+        h.update(os.path.relpath(f, ROOT).encode())   # the tree may move (another checkout)
         with open(f, "rb") as fh:
             h.update(fh.read())
     h.update(" ".join(NVCC_FLAGS).encode())

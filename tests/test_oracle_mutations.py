@@ -13,12 +13,14 @@ import pytest
 import oracle.attention as oatt
 import oracle.draft_sample as odraft
 import oracle.kv_cache as okv
+import oracle.scheduler as osched
 import oracle.philox as ophil
 import oracle.selection as osel
 import oracle.spec_sample  # noqa: F401  (the package re-exports a function of the same name)
 import test_oracle_attention as pins_att
 import test_oracle_draft_sample as pins_draft
 import test_oracle_kv_cache as pins_kv
+import test_oracle_scheduler as pins_sched
 import test_oracle_philox as pins_phil
 import test_oracle_select as pins_sel
 import test_oracle_spec_sample as pins_spec
@@ -137,3 +139,16 @@ def test_commit_without_the_pending_token_is_caught(monkeypatch):
                      "np.asarray(n_accepted, dtype=np.int64)")
     monkeypatch.setattr(pins_kv, "commit_lengths", mutant)
     _fails(pins_kv.test_commit_closed_form)
+
+
+def test_aimd_blind_to_the_backlog_is_caught(monkeypatch):
+    mutant = _mutant(osched, "simulate", 'if util > cfg["util_high"] or len(paused) > cfg["backlog_max"]:',
+                     'if util > cfg["util_high"]:')
+    monkeypatch.setattr(pins_sched, "simulate", mutant)
+    _fails(pins_sched.test_multiplicative_cut_closed_form)
+
+
+def test_new_requests_ahead_of_paused_ones_is_caught(monkeypatch):
+    mutant = _mutant(osched, "simulate", "            if paused:\n", "            if paused and not waiting:\n")
+    monkeypatch.setattr(pins_sched, "simulate", mutant)
+    _fails(pins_sched.test_invariants_on_random_workloads, osched.POLICY_AIMD, 1)

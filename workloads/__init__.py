@@ -9,6 +9,7 @@ arithmetic.
 from .configs import ATTN_CONFIGS, SAMPLER_CONFIGS, AttnConfig, SamplerConfig
 from .attention_inputs import PagedKV, make_paged_kv, make_queries, bf16_to_bits
 from .sampler_inputs import SpecInputs, make_spec_inputs
+from .scheduler_inputs import RolloutRequests, make_rollout_requests
 
 __all__ = [
     "ATTN_CONFIGS",
@@ -21,4 +22,6 @@ __all__ = [
     "bf16_to_bits",
     "SpecInputs",
     "make_spec_inputs",
+    "RolloutRequests",
+    "make_rollout_requests",
 ]
