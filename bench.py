@@ -879,6 +879,100 @@ def run_layers(args):
             "launches_per_dense_4_steps": k * (2 * n_layers + 1), "clocks": clock_info}
 
 
+def run_speedup(args):
+    """Speedup-model calibration on measured kernel times: Qwen3-8B attention
+    geometry, one layer, 128 sequences x U{8192..24576}, k = 8, V = 151936.
+    A dense step is dense decode attention plus sampling one token from p; an
+    S3R round at budget b is k x (sparse draft attention + draft-token
+    sampling) + verify with page mass + exact speculative sampling + page
+    selection.  Each is timed as a whole (gigabytes per iteration, above L2).
+    rho(b) = draft KV bytes per step / dense KV bytes per step (algorithmic);
+    cost(b) = T_round(b) / T_dense.  The constant correction is fitted on
+    alternate budgets and judged on the others."""
+    import speculative_decode_attention_paged_b300 as s3r
+    from speculative_decode_attention_paged_b300 import speedup_model as sm
+    dev = torch.device("cuda", torch.cuda.current_device())
+    c = ATTN_CONFIGS[3]
+    sc = SAMPLER_CONFIGS[2]
+    S = args.seqs or c.num_seqs
+    k, Hq, Hkv = c.k, c.q_heads, c.kv_heads
+    kv = make_paged_kv(S, Hq, Hkv, 2 * k, seed=c.seed, device=dev, hist_min=c.hist_min, hist_max=c.hist_max)
+    desc = s3r.PagedKVDesc(kv.k_pool, kv.v_pool, kv.block_table, Hq)
+    ws = s3r.Workspace(s3r.s3r_attn_workspace_size(desc, k), device=dev)
+    L = kv.hist_lens
+    qv = make_queries(kv, 3000, rows=k)
+    qd = [make_queries(kv, 3100 + j) for j in range(k)]
+    out_v = torch.empty(qv.shape, dtype=torch.float32, device=dev)
+    out_d = torch.empty(qd[0].shape, dtype=torch.float32, device=dev)
+    mass = torch.empty((S, Hkv, kv.max_pages), dtype=torch.float32, device=dev)
+    sel_lens = (L + k).to(torch.int32)
+    ctx = (L + 1).to(torch.int32)
+    spec = make_spec_inputs(S, k, sc.vocab, sc.p_sigma, sc.q_sigmas[0], sc.seed, device=dev)
+    drafts = torch.empty((S, k), dtype=torch.int32, device=dev)
+    out_t = torch.empty((S, k + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((S,), dtype=torch.int32, device=dev)
+    tok1 = torch.empty((S,), dtype=torch.int32, device=dev)
+    sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(S, k), device=dev)
+    dws = s3r.Workspace(s3r.s3r_sample_draft_workspace_size(S), device=dev)
+    s3r.s3r_verify_attn(desc, L, qv, out_v, 1.0, ws, page_mass=mass)
+    clocks = _clock_sampler()
+
+    def dense_step():
+        s3r.s3r_dense_decode_attn(desc, ctx, qd[0], out_d, 1.0, ws)
+        s3r.s3r_sample_draft_tokens(spec.p_logits[:, 0], sc.philox_seed, 0, 0, tok1, dws)
+
+    t_dense = _timed(dense_step, args.steps, args.warmup)
+    dense_kv = float((L.double() + 1).sum()) * Hkv * KV_TOKEN_BYTES_PER_HEAD
+    budgets = (0.02, 0.05, 0.10, 0.15, 0.20, 0.25, 0.35, 0.50, 0.75, 1.00)
+    rows = []
+    for b in budgets:
+        b_max = selection_budget_pages(kv.max_pages, b)
+        sel = torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev)
+        cnt = torch.empty((S, Hkv), dtype=torch.int32, device=dev)
+        s3r.s3r_select_draft_pages(mass, sel_lens, b, sel, cnt, ws)
+        draft_kv = sum(_visible_draft_tokens(sel, cnt, sel_lens, j) for j in range(k)) * KV_TOKEN_BYTES_PER_HEAD / k
+
+        def s3r_round():
+            for j in range(k):
+                s3r.s3r_sparse_draft_attn(desc, sel_lens, j, sel, cnt, qd[j], out_d, 1.0, ws)
+                s3r.s3r_sample_draft_tokens(spec.q_logits[:, j], sc.philox_seed, 0, j, drafts[:, j], dws)
+            s3r.s3r_verify_attn(desc, L, qv, out_v, 1.0, ws, page_mass=mass)
+            s3r.s3r_spec_sample(spec.p_logits, spec.q_logits, drafts, sc.philox_seed, 0, out_t, nacc, sws)
+            s3r.s3r_select_draft_pages(mass, sel_lens, b, sel, cnt, ws)
+
+        t_round = _timed(s3r_round, max(3, args.steps // 2), args.warmup)
+        rows.append({"budget": b, "rho": draft_kv / dense_kv, "round_ms": t_round, "cost": t_round / t_dense})
+    for w in (ws, sws, dws):
+        w.check()
+    clock_info = clocks.stop()
+    rho = np.array([r["rho"] for r in rows])
+    cost = np.array([r["cost"] for r in rows])
+    train = np.arange(len(rows)) % 2 == 0
+    cal = sm.calibrate(rho, cost, k, train)
+    for r in rows:
+        r["model_cost_uncorrected"] = float(sm.round_cost(r["rho"], k))
+        r["model_cost_corrected"] = float(sm.round_cost(r["rho"], k, cal["c"]))
+    a_meas = float(nacc.double().mean().item()) / k
+    # the pages' two budget points (per-position acceptance 80.4% at 0.05 and 96.7%
+    # at 0.50, draft length 6 on their system): what this build's costs predict
+    context = {}
+    for b, alpha in ((0.05, 0.804), (0.50, 0.967)):
+        i = budgets.index(b)
+        a = float(sm.accepted_prefix_fraction(alpha, k))
+        context[str(b)] = {"alpha": alpha, "accepted_prefix_fraction": a,
+                           "predicted_speedup": float(sm.predict(a, rho[i], k, cal["c"])),
+                           "measured_cost_speedup": float(sm.tokens_per_round(a, k) / cost[i])}
+    return {"workload": f"speedup-model calibration, qwen3-8b-geom 1 layer: {S} seqs x U{{8192..24576}}, k={k}, "
+                        f"V={sc.vocab}, budgets {list(budgets)}",
+            "metric": "held-out MAPE of the calibrated speedup model", "value": cal["heldout_mape_corrected"],
+            "unit": "%", "higher_is_better": False, "dense_step_ms": t_dense, "points": rows, "calibration": cal,
+            "train_budgets": [budgets[i] for i in range(len(budgets)) if train[i]],
+            "synthetic_accepted_prefix_fraction": a_meas,
+            "speedup_at_synthetic_acceptance": {str(r["budget"]): float(sm.tokens_per_round(a_meas, k) / r["cost"])
+                                                for r in rows},
+            "context_pages_budget_points": context, "clocks": clock_info}
+
+
 def _host_link_gbs():
     """Host-to-device copy rate of pinned memory (1 GiB, median of 5), or None
     without a GPU."""
@@ -981,10 +1075,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("s3r", "reference"), default="s3r")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("round", "sweep", "sampler", "layers", "scheduler"), default="round",
+    ap.add_argument("--workload", choices=("round", "sweep", "sampler", "layers", "scheduler", "speedup"),
+                    default="round",
                     help="round (default): the 256-sequence S3R round + dense baseline; sweep: Qwen3-8B "
                          "geometry budget sweep; sampler: 2048 x k=8 sampler; layers: the 28-layer closed round; "
-                         "scheduler: the AIMD KV scheduler simulation (host)")
+                         "scheduler: the AIMD KV scheduler simulation (host); speedup: the speedup-model "
+                         "calibration on measured round and dense-step times")
     ap.add_argument("--layers", type=int, default=None, help="fewer layers for --workload layers")
     ap.add_argument("--all-16k", action="store_true", help="--workload layers with every history at 16K")
     ap.add_argument("--seqs", type=int, default=None,
@@ -1000,7 +1096,7 @@ def main(argv=None):
             import speculative_decode_attention_paged_b300 as s3r
             s3r.load_library()
             leg = {"sweep": run_sweep, "sampler": run_sampler, "layers": run_layers,
-                   "scheduler": run_scheduler}[args.workload]
+                   "scheduler": run_scheduler, "speedup": run_speedup}[args.workload]
             line = leg(args)
             line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
                          "data": "synthetic", "l2": "inputs larger than L2"})
