@@ -39,8 +39,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import (ATTN_CONFIGS, SAMPLER_CONFIGS, make_paged_kv, make_queries, make_rollout_requests,  # noqa: E402
-                       make_spec_inputs)
+from workloads import (ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_1P7B_28LAYER, ATTN_QWEN3_8B_128SEQ,  # noqa: E402
+                       SAMPLER_ROLLOUT_2048SEQ, SAMPLER_ROUND_256SEQ, make_paged_kv, make_queries,
+                       make_rollout_requests, make_spec_inputs)
 
 METRIC = "KV GB/s (% of 8 TB/s) and draft+verify attention tokens/s at 1 B300"
 UNIT = "GB/s"
@@ -65,9 +66,9 @@ def selection_budget_pages(P, budget, n_sink=1, n_recent=4):
 class Workload:
     """Device-resident inputs of one step (built once, reused every step)."""
 
-    def __init__(self, device, attn_cfg=2, sampler_cfg=2, num_seqs=None):
-        self.cfg = ATTN_CONFIGS[attn_cfg]
-        self.scfg = SAMPLER_CONFIGS[sampler_cfg]
+    def __init__(self, device, attn_cfg=ATTN_QWEN3_1P7B_256SEQ, sampler_cfg=SAMPLER_ROUND_256SEQ, num_seqs=None):
+        self.cfg = attn_cfg
+        self.scfg = sampler_cfg
         if num_seqs is not None:
             import dataclasses
             self.cfg = dataclasses.replace(self.cfg, num_seqs=int(num_seqs))
@@ -307,8 +308,8 @@ def oracle_sample(seconds, seed=0):
     import oracle
     from workloads import bf16_to_bits
 
-    c = ATTN_CONFIGS[2]
-    sc = SAMPLER_CONFIGS[2]
+    c = ATTN_QWEN3_1P7B_256SEQ
+    sc = SAMPLER_ROUND_256SEQ
     n_seqs = 8
     if seed not in _ORACLE_INPUTS:
         _ORACLE_INPUTS.clear()
@@ -683,7 +684,7 @@ def run_sweep(args):
     0.50}: select + 8 sparse draft steps."""
     import speculative_decode_attention_paged_b300 as s3r
     dev = torch.device("cuda", torch.cuda.current_device())
-    c = ATTN_CONFIGS[3]
+    c = ATTN_QWEN3_8B_128SEQ
     S = args.seqs or c.num_seqs
     kv = make_paged_kv(S, c.q_heads, c.kv_heads, 2 * c.k, seed=c.seed, device=dev,
                        hist_min=c.hist_min, hist_max=c.hist_max)
@@ -743,7 +744,7 @@ def run_sampler(args):
     x 8 responses) x k = 8 over V = 151936, sigma in {0.3, 1.0}."""
     import speculative_decode_attention_paged_b300 as s3r
     dev = torch.device("cuda", torch.cuda.current_device())
-    sc = SAMPLER_CONFIGS[4]
+    sc = SAMPLER_ROLLOUT_2048SEQ
     N = args.seqs or sc.num_seqs
     res = {}
     for sigma in sc.q_sigmas:
@@ -817,8 +818,8 @@ def run_layers(args):
     the same slots), so each timed step is the same round."""
     import speculative_decode_attention_paged_b300 as s3r
     dev = torch.device("cuda", torch.cuda.current_device())
-    c = ATTN_CONFIGS[5]
-    sc = SAMPLER_CONFIGS[2]
+    c = ATTN_QWEN3_1P7B_28LAYER
+    sc = SAMPLER_ROUND_256SEQ
     S, k, Hq, Hkv, n_layers = (args.seqs or c.num_seqs), c.k, c.q_heads, c.kv_heads, c.layers
     if args.layers:
         n_layers = args.layers
@@ -961,8 +962,8 @@ def run_speedup(args):
     import speculative_decode_attention_paged_b300 as s3r
     from speculative_decode_attention_paged_b300 import speedup_model as sm
     dev = torch.device("cuda", torch.cuda.current_device())
-    c = ATTN_CONFIGS[3]
-    sc = SAMPLER_CONFIGS[2]
+    c = ATTN_QWEN3_8B_128SEQ
+    sc = SAMPLER_ROUND_256SEQ
     S = args.seqs or c.num_seqs
     k, Hq, Hkv = c.k, c.q_heads, c.kv_heads
     kv = make_paged_kv(S, Hq, Hkv, 2 * k, seed=c.seed, device=dev, hist_min=c.hist_min, hist_max=c.hist_max)
@@ -1023,7 +1024,7 @@ def run_speedup(args):
         r["model_cost_corrected"] = float(sm.round_cost(r["rho"], k, cal["c"]))
     a_meas = float(nacc.double().mean().item()) / k
     # the pages' two budget points (per-position acceptance 80.4% at 0.05 and 96.7%
-    # at 0.50, draft length 6 on their system): what this build's costs predict
+    # at 0.50, draft length 6 on their system): what the measured costs predict
     context = {}
     for b, alpha in ((0.05, 0.804), (0.50, 0.967)):
         i = budgets.index(b)

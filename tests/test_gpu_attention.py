@@ -14,7 +14,8 @@ import torch
 
 import oracle
 import speculative_decode_attention_paged_b300 as s3r
-from workloads import ATTN_CONFIGS, make_paged_kv, make_queries, bf16_to_bits
+from workloads import (ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_8B_128SEQ, ATTN_TINY, bf16_to_bits, make_paged_kv,
+                       make_queries)
 from helpers import (assert_attn_close, attn_workspace, compact_pool, host, kv_desc, run_verify_select)
 
 pytestmark = pytest.mark.gpu
@@ -196,8 +197,7 @@ def test_sm_scale_is_applied():
 
 # ---------------------------------------------------------------- the workloads at full size
 
-def _full_round_check(cfg_id, budget, n_check, seed_q=500):
-    cfg = ATTN_CONFIGS[cfg_id]
+def _full_round_check(cfg, budget, n_check, seed_q=500):
     # capacity for the verified block and the next round's draft tail
     kv = make_paged_kv(cfg.num_seqs, cfg.q_heads, cfg.kv_heads, 2 * cfg.k, seed=cfg.seed, device=DEV,
                        hist_min=cfg.hist_min, hist_max=cfg.hist_max)
@@ -223,11 +223,11 @@ def _full_round_check(cfg_id, budget, n_check, seed_q=500):
     G = cfg.q_heads // cfg.kv_heads
     np.testing.assert_allclose(host(mass).astype(np.float64).sum(axis=-1), G * T, rtol=1e-4)
 
-    seqs = sorted(np.random.default_rng(cfg_id).choice(cfg.num_seqs, size=n_check, replace=False).tolist())
+    seqs = sorted(np.random.default_rng(cfg.seed).choice(cfg.num_seqs, size=n_check, replace=False).tolist())
     kp, vp, bt = compact_pool(kv, seqs)
     Ls = host(kv.hist_lens)[seqs]
     ref_v, mref = oracle.verify_attn(bf16_to_bits(qv[seqs]), kp, vp, bt, Ls, 1.0)
-    assert_attn_close(out_v[seqs], ref_v, f"cfg{cfg_id} verify")
+    assert_attn_close(out_v[seqs], ref_v, f"{cfg.name} verify")
     _check_mass(mass[seqs], mref, G * T)
     # selection from the GPU mass equals the oracle rule applied to the same mass
     sel_ref, cnt_ref = oracle.select_draft_pages(host(mass[seqs]), host(sel_lens)[seqs], budget, 1, 4,
@@ -237,19 +237,19 @@ def _full_round_check(cfg_id, budget, n_check, seed_q=500):
     for j in range(T):
         ref_d = oracle.sparse_draft_attn(bf16_to_bits(qd[j][seqs]), kp, vp, bt, host(kv2_hist)[seqs], j,
                                          host(sel[seqs]), host(cnt[seqs]), 1.0)
-        assert_attn_close(outs_d[j][seqs], ref_d, f"cfg{cfg_id} draft j={j}")
+        assert_attn_close(outs_d[j][seqs], ref_d, f"{cfg.name} draft j={j}")
     ref_dense = oracle.dense_decode_attn(bf16_to_bits(qdense[seqs]), kp, vp, bt, Ls + 1, 1.0)
-    assert_attn_close(out_dense[seqs], ref_dense, f"cfg{cfg_id} dense")
+    assert_attn_close(out_dense[seqs], ref_dense, f"{cfg.name} dense")
 
 
-def test_config1_tiny_full():
-    _full_round_check(1, 0.10, n_check=4)
+def test_tiny_workload_full():
+    _full_round_check(ATTN_TINY, 0.10, n_check=4)
 
 
-def test_config2_qwen3_1p7b_geometry_sampled():
-    _full_round_check(2, 0.05, n_check=5)
+def test_qwen3_1p7b_256seq_sampled():
+    _full_round_check(ATTN_QWEN3_1P7B_256SEQ, 0.05, n_check=5)
 
 
 @pytest.mark.parametrize("budget", [0.05, 0.50])
-def test_config3_qwen3_8b_geometry_sampled(budget):
-    _full_round_check(3, budget, n_check=3)
+def test_qwen3_8b_128seq_sampled(budget):
+    _full_round_check(ATTN_QWEN3_8B_128SEQ, budget, n_check=3)

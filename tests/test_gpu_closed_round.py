@@ -7,7 +7,7 @@ stage against the oracle on the inputs each GPU stage consumed:
   exact speculative sampling; length commit L' = L + n_acc + 1; selection of
   the next round's pages from the verify mass over L'.
 
-Round 2 starts from round 1's L' and selection.  Pools are compared bit for
+The second round starts from the first round's L' and selection.  Pools are compared bit for
 bit, attention with the attention tolerances, page mass with the mass
 tolerance, tokens and accepted counts exactly up to the sampler's tie rules,
 lengths and selections exactly (the selection oracle reads the GPU's fp32

@@ -17,7 +17,7 @@ from scipy import special, stats
 
 import oracle
 import speculative_decode_attention_paged_b300 as s3r
-from workloads import SAMPLER_CONFIGS, make_spec_inputs
+from workloads import SAMPLER_ROLLOUT_2048SEQ, SAMPLER_TINY, make_spec_inputs
 from helpers import host
 
 pytestmark = pytest.mark.gpu
@@ -70,8 +70,8 @@ def compare(p_logits, q_logits, drafts, seed, offset, out_g, nacc_g, max_tie_fra
     return ratio_ties, cdf_ties
 
 
-def test_config1_tiny_full():
-    cfg = SAMPLER_CONFIGS[1]
+def test_tiny_sampler_full():
+    cfg = SAMPLER_TINY
     inp = make_spec_inputs(cfg.num_seqs, cfg.k, cfg.vocab, cfg.p_sigma, cfg.q_sigmas[0], cfg.seed, device=DEV)
     out, nacc = _gpu(inp, cfg.philox_seed)
     compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), cfg.philox_seed, 0, out, nacc)
@@ -105,8 +105,8 @@ def test_k_zero_samples_bonus_only():
     compare(host(inp.p_logits), host(inp.q_logits), host(inp.draft_tokens), 6, 0, out, nacc)
 
 
-def test_config4_rollout_scale_sampled():
-    cfg = SAMPLER_CONFIGS[4]
+def test_rollout_2048seq_sampled():
+    cfg = SAMPLER_ROLLOUT_2048SEQ
     for sigma in cfg.q_sigmas:
         inp = make_spec_inputs(cfg.num_seqs, cfg.k, cfg.vocab, cfg.p_sigma, sigma, cfg.seed, device=DEV)
         out, nacc = _gpu(inp, cfg.philox_seed)

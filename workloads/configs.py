@@ -1,4 +1,4 @@
-"""The five workloads, by what they are and their sizes.
+"""The workloads, each named by what it is and its sizes.
 
 Shapes follow the S³R pages' rollout setting: Qwen3-1.7B / Qwen3-8B attention
 geometry, 16K / 24K maximum responses, 256 prompts x 8 responses, the 151936
@@ -41,25 +41,26 @@ class SamplerConfig:
     philox_seed: int = 0
 
 
-ATTN_CONFIGS = {
-    1: AttnConfig("tiny-1layer-4x2048", num_seqs=4, hist_min=2048, hist_max=2048,
-                  q_heads=16, kv_heads=8, k=4, budgets=(0.10,), seed=1),
-    2: AttnConfig("qwen3-1.7b-geom-256seq-4k16k", num_seqs=256, hist_min=4096, hist_max=16384,
-                  q_heads=16, kv_heads=8, k=4, budgets=(0.05,), seed=2),
-    3: AttnConfig("qwen3-8b-geom-128seq-8k24k", num_seqs=128, hist_min=8192, hist_max=24576,
-                  q_heads=32, kv_heads=8, k=8, budgets=(0.05, 0.10, 0.25, 0.50), seed=3),
-    5: AttnConfig("qwen3-1.7b-geom-28layer-32seq-4k16k", num_seqs=32, hist_min=4096, hist_max=16384,
-                  q_heads=16, kv_heads=8, k=4, budgets=(0.05,), seed=5, layers=28,
-                  capacity_tokens=16384),
-}
+# Attention workloads.
+ATTN_TINY = AttnConfig("tiny-1layer-4x2048", num_seqs=4, hist_min=2048, hist_max=2048,
+                       q_heads=16, kv_heads=8, k=4, budgets=(0.10,), seed=1)
+ATTN_QWEN3_1P7B_256SEQ = AttnConfig("qwen3-1.7b-geom-256seq-4k16k", num_seqs=256, hist_min=4096, hist_max=16384,
+                                    q_heads=16, kv_heads=8, k=4, budgets=(0.05,), seed=2)
+ATTN_QWEN3_8B_128SEQ = AttnConfig("qwen3-8b-geom-128seq-8k24k", num_seqs=128, hist_min=8192, hist_max=24576,
+                                  q_heads=32, kv_heads=8, k=8, budgets=(0.05, 0.10, 0.25, 0.50), seed=3)
+ATTN_QWEN3_1P7B_28LAYER = AttnConfig("qwen3-1.7b-geom-28layer-32seq-4k16k", num_seqs=32, hist_min=4096,
+                                     hist_max=16384, q_heads=16, kv_heads=8, k=4, budgets=(0.05,), seed=5,
+                                     layers=28, capacity_tokens=16384)
 
-SAMPLER_CONFIGS = {
-    1: SamplerConfig("tiny-4seq-k4-v4096", num_seqs=4, k=4, vocab=4096, p_sigma=3.0,
-                     q_sigmas=(0.5,), seed=1),
-    # The sampler leg of the one-layer round (sequences of the 1.7B-geometry
-    # workload, k = 4, Qwen3 vocabulary, sigma = 1.0 gives ~80% acceptance).
-    2: SamplerConfig("round-256seq-k4-v151936", num_seqs=256, k=4, vocab=151936, p_sigma=3.0,
-                     q_sigmas=(1.0,), seed=2),
-    4: SamplerConfig("rollout-2048seq-k8-v151936", num_seqs=2048, k=8, vocab=151936, p_sigma=3.0,
-                     q_sigmas=(0.3, 1.0), seed=4),
-}
+# Sampler workloads.
+SAMPLER_TINY = SamplerConfig("tiny-4seq-k4-v4096", num_seqs=4, k=4, vocab=4096, p_sigma=3.0,
+                             q_sigmas=(0.5,), seed=1)
+# The sampler leg of the one-layer round (sequences of the 1.7B-geometry
+# workload, k = 4, Qwen3 vocabulary, sigma = 1.0).
+SAMPLER_ROUND_256SEQ = SamplerConfig("round-256seq-k4-v151936", num_seqs=256, k=4, vocab=151936, p_sigma=3.0,
+                                     q_sigmas=(1.0,), seed=2)
+SAMPLER_ROLLOUT_2048SEQ = SamplerConfig("rollout-2048seq-k8-v151936", num_seqs=2048, k=8, vocab=151936,
+                                        p_sigma=3.0, q_sigmas=(0.3, 1.0), seed=4)
+
+ATTN_CONFIGS = {c.name: c for c in (ATTN_TINY, ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_8B_128SEQ, ATTN_QWEN3_1P7B_28LAYER)}
+SAMPLER_CONFIGS = {c.name: c for c in (SAMPLER_TINY, SAMPLER_ROUND_256SEQ, SAMPLER_ROLLOUT_2048SEQ)}
