@@ -15,12 +15,21 @@ vocabulary 151936 for the sampler):
   5. exact speculative sampling of the 256 drafted blocks.
 
 `value` is the algorithmic HBM throughput of the whole step in GB/s (KV bytes
-of every attention call + queries/outputs + page mass + selection + logits,
-section "Bytes" of the design notes) divided by the device time of the step;
-the per-phase split, the draft+verify attention tokens/s, the dense tokens/s
-and the effective tokens/s at the measured acceptance are extra keys.  The
-reference arm (--impl reference) times the fp64 CPU oracle on a bounded sample
-of the same workload.
+of every attention call + queries/outputs + page mass + selection + logits:
+the bytes the step must move at least once) divided by the device time of the
+step; the per-phase split, the draft+verify attention tokens/s, the dense
+tokens/s and the effective tokens/s at the measured acceptance are extra keys.
+`e2e` repeats the step through the same calls with host inputs and results:
+each step's inputs are copied from pinned host memory and its results copied
+back inside the timed region, two buffer sets letting one step's upload
+overlap the previous step's kernels.  The reference arm (--impl reference)
+times the fp64 CPU oracle on a bounded sample of the same workload.
+
+Other workloads (--workload, one JSON line each): `sweep` (Qwen3-8B geometry,
+budgets 0.05 .. 0.50), `sampler` (2048 sequences x k = 8, parallel and
+sequential samplers, draft-token sampling), `layers` (the closed 28-layer
+round against 4 dense steps), `scheduler` (the AIMD KV scheduler simulation,
+host only) and `speedup` (the speedup-model calibration).
 """
 
 import argparse

@@ -18,8 +18,8 @@ What the pages fix
   ([ritwork] "Как разреженный черновик ...", last paragraph).  The page mass
   returned by ``verify_attn`` is that signal.
 
-Readings where the pages are silent (each listed in the design doc)
---------------------------------------------------------------
+Readings where the pages are silent
+-----------------------------------
 * Attention is softmax(sm_scale * q.K^T) V per query head; query head qh uses
   KV head qh // G (contiguous GQA groups).
 * KV cache pages hold 16 tokens; pool layout [page][kv_head][16][head_dim].

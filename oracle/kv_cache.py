@@ -14,8 +14,8 @@ What the pages fix
   after it are dropped, and a corrected token takes its place ([rebas]
   "草稿可以稀疏，交卷必须完整"; [ritwork] same section).
 
-Readings where the pages are silent (each listed in the design doc)
---------------------------------------------------------------
+Readings where the pages are silent
+-----------------------------------
 * Block row t of sequence s is the token at position L + t, stored in slot
   (L + t) % 16 of the sequence's logical page (L + t) // 16, i.e. of physical
   page block_table[s][(L + t) // 16] (the cache layout of attention.py).

@@ -21,8 +21,8 @@ What the pages fix
   moved per 1000 generated tokens; cumulative recompute and moved pages
   ([rebas] same section; [wispaper] "What to watch").
 
-Readings where the pages are silent (each listed in the design doc)
---------------------------------------------------------------
+Readings where the pages are silent
+-----------------------------------
 * One scheduler step is one S³R round of every running request.  Before the
   round each running request holds pages for its context plus the k + 1
   tokens the round may write: pages_for(P + g + k + 1), pages of 16 tokens.

@@ -15,7 +15,7 @@ standard one for exact speculative sampling:
   first rejection at i: emit y ~ normalize(max(0, p_i - q_i)), stop
   all k accepted: emit a bonus token y ~ p_{k+1}
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
   * temperature 1 over the full vocabulary: p_i = softmax(p_logits[i]),
     q_i = softmax(q_logits[i]);
   * accept iff u_i < p_i(x_i) / q_i(x_i) (strict), u_i the Philox uniform of

@@ -1,6 +1,6 @@
 """Paged bf16 KV pools, block tables and queries with planted heavy hitters.
 
-Recipe (stated in DESIGN.md, "Input recipe"):
+Recipe:
   * history lengths L ~ U{hist_min .. hist_max} (or given);
   * every sequence owns ceil(max(L + k, capacity) / 16) pages; the physical
     pages of the pool are a random permutation, so the block table is

@@ -1,6 +1,6 @@
 """Target / draft logits and drafted tokens for the speculative sampler.
 
-Recipe ("Input recipe"): p_logits ~ N(0, p_sigma^2) fp32 for k+1
+Recipe: p_logits ~ N(0, p_sigma^2) fp32 for k+1
 positions, q_logits = p_logits[:k] + N(0, q_sigma^2), drafted tokens
 x_i ~ softmax(q_logits[i]) drawn by the Gumbel-max trick (argmax of logits
 plus Gumbel noise), so no normalisation happens here.

@@ -1,6 +1,6 @@
 """Synthetic RL rollout requests for the scheduler simulation.
 
-Recipe (stated in DESIGN.md, "Input recipe"): n_prompts prompts of
+Recipe: n_prompts prompts of
 U{prompt_lo .. prompt_hi} tokens, each sampled `group` times (a response
 group shares its prompt); response lengths log-uniform on
 [response_lo, response_hi] (long-tailed, as in long-context reasoning);
