@@ -27,7 +27,7 @@ def _gpu(logits, seed, offset, pos):
     return host(tok)
 
 
-@pytest.mark.parametrize("n,V", [(64, 1), (64, 7), (200, 4099), (256, 4096), (128, 151936)])
+@pytest.mark.parametrize("n,V", [(64, 1), (64, 7), (200, 4099), (256, 4096), (128, 151936), (16, 300001)])
 def test_matches_oracle(n, V):
     g = torch.Generator(device=DEV)
     g.manual_seed(n * 7 + V)
