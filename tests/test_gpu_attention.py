@@ -253,3 +253,25 @@ def test_qwen3_1p7b_256seq_sampled():
 @pytest.mark.parametrize("budget", [0.05, 0.50])
 def test_qwen3_8b_128seq_sampled(budget):
     _full_round_check(ATTN_QWEN3_8B_128SEQ, budget, n_check=3)
+
+
+def test_long_context_dense_and_verify_with_mass():
+    """A 100,003-token history (6,251 pages) next to tiny ones: the page stream
+    and the split merges stay exact far beyond the workloads' lengths."""
+    lens = [100_003, 3, 17]
+    kv = make_paged_kv(len(lens), 16, 8, 4, seed=107, device=DEV, hist_lens=lens, heavy_per_head=4)
+    kp, vp, bt = _oracle_inputs(kv)
+    ws = attn_workspace(kv, rows=4)
+    qd = make_queries(kv, 11)
+    out_d = torch.empty(qd.shape, dtype=torch.float32, device=DEV)
+    s3r.s3r_dense_decode_attn(kv_desc(kv), kv.hist_lens + 1, qd, out_d, 1.0, ws)
+    qv = make_queries(kv, 12, rows=4)
+    out_v = torch.empty(qv.shape, dtype=torch.float32, device=DEV)
+    mass = torch.empty((len(lens), 8, kv.max_pages), dtype=torch.float32, device=DEV)
+    s3r.s3r_verify_attn(kv_desc(kv), kv.hist_lens, qv, out_v, 1.0, ws, page_mass=mass)
+    ws.check()
+    assert_attn_close(out_d, oracle.dense_decode_attn(bf16_to_bits(qd), kp, vp, bt, host(kv.hist_lens) + 1, 1.0),
+                      "long dense")
+    ref_v, mref = oracle.verify_attn(bf16_to_bits(qv), kp, vp, bt, host(kv.hist_lens), 1.0)
+    assert_attn_close(out_v, ref_v, "long verify")
+    _check_mass(mass, mref, 2 * 4)
