@@ -18,11 +18,26 @@ struct PairGeom {
   int cnt;    // selected pages (sparse)
 };
 
-// Pages of pair `pair` in the global stream, with its length and selection count.
-__device__ PairGeom pair_geom(const AttnArgs& a, int pair, bool report) {
+// The inputs of a pair's geometry: its sequence's length and (sparse) its
+// selection count.  Loaded apart from their use so that callers can have the
+// loads of many pairs in flight together.
+struct GeomIn {
+  int len;
+  int cnt;
+};
+
+__device__ __forceinline__ GeomIn pair_geom_load(const AttnArgs& a, int pair) {
+  GeomIn in;
+  in.len = __ldg(a.lens + pair / a.Hkv);
+  in.cnt = a.mode == kModeSparse ? __ldg(a.sel_count + pair) : 0;
+  return in;
+}
+
+// Pages of a pair in the global stream, with its length and selection count,
+// from its loaded inputs.
+__device__ PairGeom pair_geom_of(const AttnArgs& a, GeomIn in, bool report) {
   PairGeom g{0, 0, 0};
-  const int s = pair / a.Hkv;
-  const int len = __ldg(a.lens + s);
+  const int len = in.len;
   const int cap = a.max_pages * kPage;
   if (a.mode == kModeDense) {
     if (len < 0 || len > cap) {
@@ -44,7 +59,7 @@ __device__ PairGeom pair_geom(const AttnArgs& a, int pair, bool report) {
       if (report) report_error(a.err, S3R_DEVERR_BAD_LENGTH);
       return g;
     }
-    int cnt = __ldg(a.sel_count + pair);
+    int cnt = in.cnt;
     if (cnt < 0 || cnt > a.b_max) {
       if (report) report_error(a.err, S3R_DEVERR_BAD_COUNT);
       cnt = 0;
@@ -54,6 +69,11 @@ __device__ PairGeom pair_geom(const AttnArgs& a, int pair, bool report) {
     g.np = cnt + (last / kPage - len / kPage + 1);
   }
   return g;
+}
+
+// Pages of pair `pair` in the global stream, with its length and selection count.
+__device__ PairGeom pair_geom(const AttnArgs& a, int pair, bool report) {
+  return pair_geom_of(a, pair_geom_load(a, pair), report);
 }
 
 struct Entry {
@@ -203,6 +223,38 @@ __device__ void zero_pair(const AttnArgs& a, int pair) {
   if (a.page_mass != nullptr) {
     float* m = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
     for (int lp = 0; lp < a.mass_stride; ++lp) m[lp] = 0.f;
+  }
+}
+
+// Plan of a call: pages of every chunk of kPairChunk pairs into prefix[c],
+// before the exclusive scan.  Warp w of nwarps takes chunks w, w + nwarps,
+// ...; the geometry loads of kPlanBatch chunks are issued before any of them is
+// used, so their latencies overlap (a chain of one load round trip per chunk
+// was most of a call's start-up).  Pairs with nothing to read get zero
+// outputs here, each from one CTA.
+constexpr int kPlanBatch = 8;
+
+__device__ __forceinline__ void plan_chunk_pages(const AttnArgs& a, int* prefix, int warp, int nwarps, int lane) {
+  for (int c0 = warp; c0 < a.n_chunks; c0 += kPlanBatch * nwarps) {
+    GeomIn in[kPlanBatch];
+#pragma unroll
+    for (int u = 0; u < kPlanBatch; ++u) {
+      const int c = c0 + u * nwarps;
+      const int pair = c * kPairChunk + lane;
+      in[u] = (c < a.n_chunks && pair < a.n_pairs) ? pair_geom_load(a, pair) : GeomIn{0, 0};
+    }
+#pragma unroll
+    for (int u = 0; u < kPlanBatch; ++u) {
+      const int c = c0 + u * nwarps;
+      const int pair = c * kPairChunk + lane;
+      int np = 0;
+      if (c < a.n_chunks && pair < a.n_pairs) {
+        np = pair_geom_of(a, in[u], blockIdx.x == 0).np;
+        if (np == 0 && (c % static_cast<int>(gridDim.x)) == static_cast<int>(blockIdx.x)) zero_pair(a, pair);
+      }
+      np = warp_sum(np);
+      if (lane == 0 && c < a.n_chunks) prefix[c] = np;
+    }
   }
 }
 

@@ -75,17 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < kAttnWarps * kAttnStages) mbar_init(&bars[tid], 1);
 
   // ---- plan: pages per chunk of 32 pairs, then an exclusive scan
-  for (int c = warp; c < a.n_chunks; c += kAttnWarps) {
-    const int pair = c * kPairChunk + lane;
-    int np = 0;
-    if (pair < a.n_pairs) {
-      np = pair_geom(a, pair, blockIdx.x == 0).np;
-      // A pair with nothing to read gets zero rows (and zero mass) here.
-      if (np == 0 && (c % static_cast<int>(gridDim.x)) == static_cast<int>(blockIdx.x)) zero_pair(a, pair);
-    }
-    np = warp_sum(np);
-    if (lane == 0) prefix[c] = np;
-  }
+  plan_chunk_pages(a, prefix, warp, kAttnWarps, lane);
   fence_barrier_init();
   __syncthreads();
   block_exclusive_scan<kThreads>(prefix, a.n_chunks, scratch);

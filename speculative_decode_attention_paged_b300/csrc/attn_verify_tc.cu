@@ -220,16 +220,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_relinquish();
   }
   // ---- plan: pages per chunk of 32 pairs, then an exclusive scan
-  for (int c = warp; c < a.n_chunks; c += kTcThreads / 32) {
-    const int pair = c * kPairChunk + lane;
-    int np = 0;
-    if (pair < a.n_pairs) {
-      np = pair_geom(a, pair, blockIdx.x == 0).np;
-      if (np == 0 && (c % static_cast<int>(gridDim.x)) == static_cast<int>(blockIdx.x)) zero_pair(a, pair);
-    }
-    np = warp_sum(np);
-    if (lane == 0) prefix[c] = np;
-  }
+  plan_chunk_pages(a, prefix, warp, kTcThreads / 32, lane);
   fence_barrier_init();
   fence_proxy_async_smem();
   tc_fence_before_sync();
