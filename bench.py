@@ -814,15 +814,16 @@ def run_layers(args):
     16K tokens per sequence (~60 GB), per-layer random queries and K/V rows,
     budget 0.05, k = 4, synthetic logits over V = 151936 (p ~ N(0, 3^2),
     q = p + N(0, 1)).  One round, captured in one CUDA graph:
-      4 draft steps: every layer appends its draft row at L + j and runs sparse
-        draft attention over the previous round's pages; the draft token is
-        sampled from q_j in place;
-      verify: every layer appends the k + 1 dense rows of [pending token,
-        drafts] at L .. L + k and verifies them with page mass;
+      4 draft steps: every layer writes its draft row at L + j and runs sparse
+        draft attention over the previous round's pages, in one launch; the
+        draft token is sampled from q_j in place;
+      verify: every layer writes the k + 1 dense rows of [pending token,
+        drafts] at L .. L + k and verifies them with page mass, in one launch;
       exact speculative sampling of the 32 blocks, the length commit
         L' = L + n_acc + 1, and every layer's pages for the next round over L'.
-    Compared with 4 dense decode steps (a second graph): every layer appends
-    the step's row and runs dense attention, then a token is sampled from p_j.
+    Compared with 4 dense decode steps (a second graph): every layer writes
+    the step's row and runs dense attention in one launch, then a token is
+    sampled from p_j.
     Both graphs restart from the same L at every replay (the appends rewrite
     the same slots), so each timed step is the same round."""
     import speculative_decode_attention_paged_b300 as s3r
@@ -870,7 +871,6 @@ def run_layers(args):
     dense_tokens = torch.empty((S, k), dtype=torch.int32, device=dev)
     Ld = L.to(dev)
     L_next = torch.empty_like(Ld)
-    starts = [(Ld + j).to(torch.int32) for j in range(k)]
     ctx = [(Ld + j + 1).to(torch.int32) for j in range(k)]
     ws = s3r.Workspace(s3r.s3r_attn_workspace_size(layers[0]["desc"], k + 1), device=dev)
     sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(S, k), device=dev)
@@ -880,12 +880,12 @@ def run_layers(args):
     def s3r_round():
         for j in range(k):
             for l in layers:
-                s3r.s3r_kv_append(l["desc"], starts[j], l["draft_kv"][j][0], l["draft_kv"][j][1], ws)
-                s3r.s3r_sparse_draft_attn(l["desc"], Ld, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0, ws)
+                s3r.s3r_sparse_draft_attn(l["desc"], Ld, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0, ws,
+                                          append=l["draft_kv"][j])
             s3r.s3r_sample_draft_tokens(spec.q_logits[:, j], sc.philox_seed, 0, j, drafts[:, j], dws)
         for l in layers:
-            s3r.s3r_kv_append(l["desc"], Ld, l["block_kv"][0], l["block_kv"][1], ws)
-            s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
+            s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"],
+                                append=l["block_kv"])
         s3r.s3r_spec_sample(spec.p_logits, spec.q_logits, drafts, sc.philox_seed, 0, out_tokens, n_acc, sws)
         s3r.s3r_commit_lengths(Ld, n_acc, k, max_len, L_next, ws)
         for l in layers:
@@ -894,8 +894,8 @@ def run_layers(args):
     def dense_steps():
         for j in range(k):
             for l in layers:
-                s3r.s3r_kv_append(l["desc"], starts[j], l["draft_kv"][j][0], l["draft_kv"][j][1], ws)
-                s3r.s3r_dense_decode_attn(l["desc"], ctx[j], l["qd"][j], l["out_d"][j], 1.0, ws)
+                s3r.s3r_dense_decode_attn(l["desc"], ctx[j], l["qd"][j], l["out_d"][j], 1.0, ws,
+                                          append=l["draft_kv"][j])
             s3r.s3r_sample_draft_tokens(spec.p_logits[:, j], sc.philox_seed, 0, j, dense_tokens[:, j], dws)
 
     # the first round's pages: a verify of the block at L, selected over L + k (a previous round)
@@ -954,8 +954,8 @@ def run_layers(args):
             "s3r_emitted_tokens_per_s": emitted / (t_round * 1e-3),
             "dense_emitted_tokens_per_s": S * k / (t_dense * 1e-3),
             "emitted_tokens_speedup": (emitted / t_round) / (S * k / t_dense),
-            "launches_per_round": n_layers * (2 * k + 3) + k + 4 + 1,
-            "launches_per_dense_4_steps": k * (2 * n_layers + 1), "clocks": clock_info}
+            "launches_per_round": n_layers * (k + 2) + k + 4 + 1,
+            "launches_per_dense_4_steps": k * (n_layers + 1), "clocks": clock_info}
 
 
 def run_speedup(args):

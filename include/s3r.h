@@ -186,6 +186,47 @@ S3R_API s3r_status s3r_verify_attn(const s3r_paged_kv* kv, const int32_t* hist_l
                            float sm_scale, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * The three attention calls above with their new K/V rows written into the
+ * pages in the same launch, before they are read: the drafter's row of the
+ * current token, and verification's dense rows of the block (wispaper.ai, "S3R
+ * drafts sparsely and verifies densely": the accepted part of the block keeps
+ * its dense states).  Each equals s3r_kv_append of those rows followed by the
+ * plain call, in results and in the pages it leaves, without the separate
+ * launch.
+ *
+ *   rows.k_rows, rows.v_rows  bf16 [num_seqs][rows.n_rows][num_kv_heads][128],
+ *                16-byte aligned
+ *   dense decode: n_rows = 1, the row of position ctx_lens[s] - 1
+ *   sparse draft: n_rows = 1, the row of position hist_lens[s] + draft_pos
+ *   verify:       n_rows = the call's n_rows, rows of positions
+ *                 hist_lens[s] .. hist_lens[s] + n_rows - 1
+ * A row whose page id is outside the pool is not written (and that page is not
+ * read: the call reports S3R_DEVERR_BAD_PAGE).  The pages that receive rows
+ * must not be shared with another sequence of the call.  The pool descriptor's
+ * k_pool and v_pool are written.
+ */
+typedef struct s3r_kv_rows {
+  const void* k_rows;
+  const void* v_rows;
+  int32_t n_rows;
+} s3r_kv_rows;
+
+S3R_API s3r_status s3r_dense_decode_attn_append(const s3r_paged_kv* kv, const int32_t* ctx_lens,
+                                        const s3r_kv_rows* rows, const void* q, void* out, float sm_scale,
+                                        void* ws, size_t ws_bytes, void* stream);
+
+S3R_API s3r_status s3r_sparse_draft_attn_append(const s3r_paged_kv* kv, const int32_t* hist_lens,
+                                        int32_t draft_pos, const int32_t* sel_pages,
+                                        const int32_t* sel_count, int32_t b_max, const s3r_kv_rows* rows,
+                                        const void* q, void* out, float sm_scale, void* ws, size_t ws_bytes,
+                                        void* stream);
+
+S3R_API s3r_status s3r_verify_attn_append(const s3r_paged_kv* kv, const int32_t* hist_lens, int32_t n_rows,
+                                  const s3r_kv_rows* rows, const void* q, void* out, float* page_mass,
+                                  int32_t mass_stride, float sm_scale, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/*
  * Choose the next draft's KV pages per (sequence, KV head) from the verify
  * page mass.  The pages say the attention scores choose the history (rit.work,
  * same section) and that selection must stay cheap (wispaper.ai, "Where the

@@ -68,6 +68,10 @@ class S3RDeviceError(RuntimeError):
         super().__init__(f"device error word 0x{code:x}")
 
 
+class _KVRows(ctypes.Structure):
+    _fields_ = [("k_rows", ctypes.c_void_p), ("v_rows", ctypes.c_void_p), ("n_rows", ctypes.c_int32)]
+
+
 class _PagedKV(ctypes.Structure):
     _fields_ = [
         ("k_pool", ctypes.c_void_p),
@@ -110,6 +114,13 @@ _SIG = {
     "s3r_sample_draft_workspace_size": (ctypes.c_int, [_I32, ctypes.POINTER(ctypes.c_size_t)]),
     "s3r_sample_draft_tokens": (ctypes.c_int, [_P, _I32, _I32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
                                                _I32, _P, ctypes.c_int64, _P, ctypes.c_size_t, _P]),
+    "s3r_dense_decode_attn_append": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, ctypes.POINTER(_KVRows), _P, _P,
+                                                    ctypes.c_float, _P, ctypes.c_size_t, _P]),
+    "s3r_sparse_draft_attn_append": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _I32, _P, _P, _I32,
+                                                    ctypes.POINTER(_KVRows), _P, _P, ctypes.c_float, _P,
+                                                    ctypes.c_size_t, _P]),
+    "s3r_verify_attn_append": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _I32, ctypes.POINTER(_KVRows), _P, _P, _P,
+                                              _I32, ctypes.c_float, _P, ctypes.c_size_t, _P]),
     "s3r_kv_append": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _P, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
     "s3r_commit_lengths": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_size_t, _P]),
 }
@@ -244,29 +255,57 @@ def s3r_select_workspace_size():
     return out.value
 
 
-def s3r_dense_decode_attn(kv: PagedKVDesc, ctx_lens, q, out, sm_scale, ws: Workspace, stream=None):
+def _rows(kv, append, n_rows):
+    """s3r_kv_rows for append = (k_rows, v_rows), bf16 [S][n_rows][Hkv][128]."""
+    k_rows, v_rows = append
+    _need(k_rows, torch.bfloat16, "append k_rows")
+    _need(v_rows, torch.bfloat16, "append v_rows")
+    if k_rows.shape != v_rows.shape or tuple(k_rows.shape) != (kv.num_seqs, n_rows, kv.num_kv_heads, 128):
+        raise ValueError(f"append rows must both be [num_seqs][{n_rows}][num_kv_heads][128]")
+    return _KVRows(k_rows.data_ptr(), v_rows.data_ptr(), n_rows)
+
+
+def s3r_dense_decode_attn(kv: PagedKVDesc, ctx_lens, q, out, sm_scale, ws: Workspace, stream=None, append=None):
+    """Dense decode; append=(k_rows, v_rows) [S][1][Hkv][128] first writes the
+    row of position ctx_len - 1 into the pages, in the same launch."""
     _need(ctx_lens, torch.int32, "ctx_lens")
     _need(q, torch.bfloat16, "q")
     _need(out, torch.float32, "out")
-    _call("s3r_dense_decode_attn", ctypes.byref(kv.c), _ptr(ctx_lens), _ptr(q), _ptr(out),
-          ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    if append is None:
+        _call("s3r_dense_decode_attn", ctypes.byref(kv.c), _ptr(ctx_lens), _ptr(q), _ptr(out),
+              ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    else:
+        rows = _rows(kv, append, 1)
+        _call("s3r_dense_decode_attn_append", ctypes.byref(kv.c), _ptr(ctx_lens), ctypes.byref(rows), _ptr(q),
+              _ptr(out), ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
     return out
 
 
 def s3r_sparse_draft_attn(kv: PagedKVDesc, hist_lens, draft_pos, sel_pages, sel_count, q, out, sm_scale,
-                          ws: Workspace, stream=None):
+                          ws: Workspace, stream=None, append=None):
+    """Sparse draft step; append=(k_rows, v_rows) [S][1][Hkv][128] first
+    writes the row of position hist_len + draft_pos, in the same launch."""
     _need(hist_lens, torch.int32, "hist_lens")
     _need(sel_pages, torch.int32, "sel_pages")
     _need(sel_count, torch.int32, "sel_count")
     _need(q, torch.bfloat16, "q")
     _need(out, torch.float32, "out")
-    _call("s3r_sparse_draft_attn", ctypes.byref(kv.c), _ptr(hist_lens), _I32(draft_pos), _ptr(sel_pages),
-          _ptr(sel_count), _I32(sel_pages.shape[-1]), _ptr(q), _ptr(out), ctypes.c_float(sm_scale),
-          ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    if append is None:
+        _call("s3r_sparse_draft_attn", ctypes.byref(kv.c), _ptr(hist_lens), _I32(draft_pos), _ptr(sel_pages),
+              _ptr(sel_count), _I32(sel_pages.shape[-1]), _ptr(q), _ptr(out), ctypes.c_float(sm_scale),
+              ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
+    else:
+        rows = _rows(kv, append, 1)
+        _call("s3r_sparse_draft_attn_append", ctypes.byref(kv.c), _ptr(hist_lens), _I32(draft_pos),
+              _ptr(sel_pages), _ptr(sel_count), _I32(sel_pages.shape[-1]), ctypes.byref(rows), _ptr(q), _ptr(out),
+              ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
     return out
 
 
-def s3r_verify_attn(kv: PagedKVDesc, hist_lens, q, out, sm_scale, ws: Workspace, page_mass=None, stream=None):
+def s3r_verify_attn(kv: PagedKVDesc, hist_lens, q, out, sm_scale, ws: Workspace, page_mass=None, stream=None,
+                    append=None):
+    """Verify of T = q.shape[1] rows; append=(k_rows, v_rows) [S][T][Hkv][128]
+    first writes the block's rows at positions hist_len .. hist_len + T - 1."""
     _need(hist_lens, torch.int32, "hist_lens")
     _need(q, torch.bfloat16, "q")
     _need(out, torch.float32, "out")
@@ -274,9 +313,15 @@ def s3r_verify_attn(kv: PagedKVDesc, hist_lens, q, out, sm_scale, ws: Workspace,
     if page_mass is not None:
         _need(page_mass, torch.float32, "page_mass")
         stride = page_mass.shape[-1]
-    _call("s3r_verify_attn", ctypes.byref(kv.c), _ptr(hist_lens), _I32(q.shape[1]), _ptr(q), _ptr(out),
-          _ptr(page_mass), _I32(stride), ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes),
-          _stream(stream))
+    if append is None:
+        _call("s3r_verify_attn", ctypes.byref(kv.c), _ptr(hist_lens), _I32(q.shape[1]), _ptr(q), _ptr(out),
+              _ptr(page_mass), _I32(stride), ctypes.c_float(sm_scale), ws.ptr(), ctypes.c_size_t(ws.nbytes),
+              _stream(stream))
+    else:
+        rows = _rows(kv, append, q.shape[1])
+        _call("s3r_verify_attn_append", ctypes.byref(kv.c), _ptr(hist_lens), _I32(q.shape[1]), ctypes.byref(rows),
+              _ptr(q), _ptr(out), _ptr(page_mass), _I32(stride), ctypes.c_float(sm_scale), ws.ptr(),
+              ctypes.c_size_t(ws.nbytes), _stream(stream))
     return out
 
 

@@ -131,7 +131,8 @@ s3r_status to_status(cudaError_t e) { return e == cudaSuccess ? S3R_OK : S3R_ERR
 s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, int T,
                          int draft_pos, const int32_t* sel_pages, const int32_t* sel_count,
                          int b_max, const void* q, void* out, float* page_mass, int mass_stride,
-                         float sm_scale, void* ws, size_t ws_bytes, void* stream) {
+                         float sm_scale, void* ws, size_t ws_bytes, void* stream,
+                         const s3r_kv_rows* rows = nullptr) {
   s3r_status st = validate_kv(kv);
   if (st != S3R_OK) return st;
   if (!std::isfinite(sm_scale)) return S3R_ERR_INVALID_ARG;
@@ -149,6 +150,11 @@ s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, 
   }
   const bool mass = page_mass != nullptr;
   if (mass && mass_stride < kv->max_pages_per_seq) return S3R_ERR_INVALID_ARG;
+  if (rows != nullptr) {
+    if (rows->n_rows != (mode == kModeVerify ? T : 1)) return S3R_ERR_INVALID_ARG;
+    if (rows->k_rows == nullptr || rows->v_rows == nullptr) return S3R_ERR_INVALID_ARG;
+    if (!aligned16(rows->k_rows) || !aligned16(rows->v_rows)) return S3R_ERR_INVALID_ARG;
+  }
 
   const int sms = current_sm_count();
   if (sms <= 0) return S3R_ERR_CUDA;
@@ -190,6 +196,14 @@ s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, 
   a.part_o = reinterpret_cast<float*>(w + lay.part_o_off);
   a.part_ml = reinterpret_cast<float*>(w + lay.part_ml_off);
   a.page_lse = mass ? reinterpret_cast<float*>(w + lay.page_lse_off) : nullptr;
+  if (rows != nullptr) {
+    a.app_k = static_cast<const uint4*>(rows->k_rows);
+    a.app_v = static_cast<const uint4*>(rows->v_rows);
+    a.app_rows = rows->n_rows;
+    // the pools are declared const in s3r_paged_kv because plain attention only reads them
+    a.k_pool_w = static_cast<uint4*>(const_cast<void*>(kv->k_pool));
+    a.v_pool_w = static_cast<uint4*>(const_cast<void*>(kv->v_pool));
+  }
   a.total_warps = total_warps;
   a.n_pairs = n_pairs;
   a.n_chunks = (n_pairs + kPairChunk - 1) / kPairChunk;
@@ -292,6 +306,31 @@ s3r_status s3r_verify_attn(const s3r_paged_kv* kv, const int32_t* hist_lens, int
                            float sm_scale, void* ws, size_t ws_bytes, void* stream) {
   return run_attention(kv, kModeVerify, hist_lens, n_rows, 0, nullptr, nullptr, 0, q, out,
                        page_mass, mass_stride, sm_scale, ws, ws_bytes, stream);
+}
+
+s3r_status s3r_dense_decode_attn_append(const s3r_paged_kv* kv, const int32_t* ctx_lens, const s3r_kv_rows* rows,
+                                        const void* q, void* out, float sm_scale, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  if (rows == nullptr) return S3R_ERR_INVALID_ARG;
+  return run_attention(kv, kModeDense, ctx_lens, 1, 0, nullptr, nullptr, 0, q, out, nullptr, 0, sm_scale, ws,
+                       ws_bytes, stream, rows);
+}
+
+s3r_status s3r_sparse_draft_attn_append(const s3r_paged_kv* kv, const int32_t* hist_lens, int32_t draft_pos,
+                                        const int32_t* sel_pages, const int32_t* sel_count, int32_t b_max,
+                                        const s3r_kv_rows* rows, const void* q, void* out, float sm_scale,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  if (rows == nullptr) return S3R_ERR_INVALID_ARG;
+  return run_attention(kv, kModeSparse, hist_lens, 1, draft_pos, sel_pages, sel_count, b_max, q, out, nullptr, 0,
+                       sm_scale, ws, ws_bytes, stream, rows);
+}
+
+s3r_status s3r_verify_attn_append(const s3r_paged_kv* kv, const int32_t* hist_lens, int32_t n_rows,
+                                  const s3r_kv_rows* rows, const void* q, void* out, float* page_mass,
+                                  int32_t mass_stride, float sm_scale, void* ws, size_t ws_bytes, void* stream) {
+  if (rows == nullptr) return S3R_ERR_INVALID_ARG;
+  return run_attention(kv, kModeVerify, hist_lens, n_rows, 0, nullptr, nullptr, 0, q, out, page_mass, mass_stride,
+                       sm_scale, ws, ws_bytes, stream, rows);
 }
 
 s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t* sel_lens, int32_t num_seqs,

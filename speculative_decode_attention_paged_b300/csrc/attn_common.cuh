@@ -226,6 +226,28 @@ __device__ void zero_pair(const AttnArgs& a, int pair) {
   }
 }
 
+// The call's appended rows that fall in logical page lp of pair (s, h), whose
+// physical page is phys: written into the pool by the whole warp (lanes 0-15
+// the K row, lanes 16-31 the V row, 16 bytes each), then ordered before the
+// TMA load of that page that this warp issues next.  A pair's page is read by
+// one warp only, so no other reader can see the page before the rows land.
+__device__ __forceinline__ void append_rows_in_page(const AttnArgs& a, int s, int h, int L, int lp, int phys,
+                                                    int lane) {
+  if (a.app_rows == 0 || phys < 0) return;
+  const int p0 = a.mode == kModeDense ? L - 1 : (a.mode == kModeSparse ? L + a.draft_pos : L);
+  const int lo = max(p0, lp * kPage), hi = min(p0 + a.app_rows, (lp + 1) * kPage);
+  if (lo >= hi) return;
+  const int piece = lane & 15;
+  const uint4* src = lane < 16 ? a.app_k : a.app_v;
+  uint4* dst = lane < 16 ? a.k_pool_w : a.v_pool_w;
+  for (int pos = lo; pos < hi; ++pos) {
+    const uint4 v = __ldg(src + ((static_cast<int64_t>(s) * a.app_rows + (pos - p0)) * a.Hkv + h) * 16 + piece);
+    dst[((static_cast<int64_t>(phys) * a.Hkv + h) * kPage + (pos % kPage)) * 16 + piece] = v;
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
 // Plan of a call: pages of every chunk of kPairChunk pairs into prefix[c],
 // before the exclusive scan.  Warp w of nwarps takes chunks w, w + nwarps,
 // ...; the geometry loads of kPlanBatch chunks are issued before any of them is

@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ehi = __shfl_sync(0xffffffffu, cache.hi, li);
     const int phys = __shfl_sync(0xffffffffu, cache.phys, li);
     const int st = static_cast<int>(pr_k % kAttnStages);
+    append_rows_in_page(a, pr_pair / a.Hkv, pr_pair % a.Hkv, pr_g.L, lp, phys, lane);
     if (lane == 0) {
       my_meta[2 * st] = make_int4(lp, elo, ehi, phys);
       my_meta[2 * st + 1] = make_int4(pr_pair, pr_e, pr_g.np, pr_g.L);

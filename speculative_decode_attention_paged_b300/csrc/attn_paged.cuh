@@ -34,6 +34,14 @@ struct AttnArgs {
   float scale_log2;                 // sm_scale * log2(e)
   float* page_mass;                 // verify only, may be null
   int mass_stride;
+  // K/V rows written into the pages before they are read (app_rows == 0: none):
+  // bf16 [S][app_rows][Hkv][128], as 16-byte pieces; the first at position
+  // ctx_len - 1 (dense), hist_len + draft_pos (sparse) or hist_len (verify)
+  const uint4* app_k;
+  const uint4* app_v;
+  int app_rows;
+  uint4* k_pool_w;                  // the pools the tensor maps read, for those writes
+  uint4* v_pool_w;
   // workspace views
   int* err;
   int* arrivals;                    // [n_pairs] segments of a cut pair published so far

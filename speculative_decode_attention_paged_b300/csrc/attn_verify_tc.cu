@@ -338,6 +338,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&k_full[st], __popc(loadmask) * 2u * kHalfBytes);
         }
         __syncwarp();
+        // appended block rows of this tile's pages, each written by the producer
+        // warp that issues the page's boxes, before it issues them
+        if (a.app_rows > 0 && (g.L + a.app_rows - 1) / kPage >= e && g.L / kPage < e + n) {
+          for (int p = pid; p < n; p += kTcProducers)
+            append_rows_in_page(a, s, h, g.L, e + p, __shfl_sync(0xffffffffu, en.phys, p), lane);
+        }
         const bool mine = load && (lane % kTcProducers) == pid;
         uint8_t* dst = stages + static_cast<size_t>(st) * kTcStageBytes + lane * kHalfBytes;
         const int y = h * kPage;
