@@ -231,6 +231,8 @@ __device__ void zero_pair(const AttnArgs& a, int pair) {
 // the K row, lanes 16-31 the V row, 16 bytes each), then ordered before the
 // TMA load of that page that this warp issues next.  A pair's page is read by
 // one warp only, so no other reader can see the page before the rows land.
+// The loads of up to kBatch rows are in flight before any of their stores.
+template <int kBatch>
 __device__ __forceinline__ void append_rows_in_page(const AttnArgs& a, int s, int h, int L, int lp, int phys,
                                                     int lane) {
   if (a.app_rows == 0 || phys < 0) return;
@@ -240,10 +242,51 @@ __device__ __forceinline__ void append_rows_in_page(const AttnArgs& a, int s, in
   const int piece = lane & 15;
   const uint4* src = lane < 16 ? a.app_k : a.app_v;
   uint4* dst = lane < 16 ? a.k_pool_w : a.v_pool_w;
-  for (int pos = lo; pos < hi; ++pos) {
-    const uint4 v = __ldg(src + ((static_cast<int64_t>(s) * a.app_rows + (pos - p0)) * a.Hkv + h) * 16 + piece);
-    dst[((static_cast<int64_t>(phys) * a.Hkv + h) * kPage + (pos % kPage)) * 16 + piece] = v;
+  for (int base = lo; base < hi; base += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int r = 0; r < kBatch; ++r) {
+      const int pos = base + r;
+      if (pos < hi) v[r] = __ldg(src + ((static_cast<int64_t>(s) * a.app_rows + (pos - p0)) * a.Hkv + h) * 16 + piece);
+    }
+#pragma unroll
+    for (int r = 0; r < kBatch; ++r) {
+      const int pos = base + r;
+      if (pos < hi) dst[((static_cast<int64_t>(phys) * a.Hkv + h) * kPage + (pos % kPage)) * 16 + piece] = v[r];
+    }
   }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
+// Lines of pair (s, h)'s appended rows (app_rows of them, 256 bytes each for K
+// and for V) into L2 when a warp starts on the pair, so the loads of
+// append_rows_in_page at the pair's tail page hit L2.
+__device__ __forceinline__ void prefetch_pair_rows(const AttnArgs& a, int s, int h, int lane) {
+  for (int i = lane; i < a.app_rows * 4; i += 32) {
+    const int t = i >> 2;
+    const uint4* src = (i & 2) ? a.app_v : a.app_k;
+    prefetch_l2(src + ((static_cast<int64_t>(s) * a.app_rows + t) * a.Hkv + h) * 16 + (i & 1) * 8);
+  }
+}
+
+// The one appended row of pair (s, h) (calls with app_rows == 1), this lane's
+// 16-byte piece of it: K for lanes 0-15, V for 16-31.  Loaded when a warp
+// starts on the pair, so the load overlaps the pair's earlier pages.
+__device__ __forceinline__ uint4 load_single_row(const AttnArgs& a, int s, int h, int lane) {
+  const uint4* src = lane < 16 ? a.app_k : a.app_v;
+  return __ldg(src + (static_cast<int64_t>(s) * a.Hkv + h) * 16 + (lane & 15));
+}
+
+// Store of that row if it falls in logical page lp (physical page phys), then
+// the same ordering before the page's TMA load as append_rows_in_page.
+__device__ __forceinline__ void store_single_row(const AttnArgs& a, int h, int L, int lp, int phys, int lane,
+                                                 uint4 v) {
+  if (phys < 0) return;
+  const int pos = a.mode == kModeDense ? L - 1 : (a.mode == kModeSparse ? L + a.draft_pos : L);
+  if (pos / kPage != lp) return;
+  uint4* dst = lane < 16 ? a.k_pool_w : a.v_pool_w;
+  dst[((static_cast<int64_t>(phys) * a.Hkv + h) * kPage + (pos % kPage)) * 16 + (lane & 15)] = v;
   fence_proxy_async_global();
   __syncwarp();
 }

@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          : Entry{-1, 0, 0, -1};
   int64_t pr_x = x0;
   int64_t pr_k = 0;
+  const bool app_one = a.app_rows == 1;
+  uint4 pr_row = app_one ? load_single_row(a, pr_pair / a.Hkv, pr_pair % a.Hkv, lane) : uint4{};
 
   auto produce = [&]() {
     if (pr_x >= x1) return;
@@ -136,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pr_e = 0;
       pr_base = 0;
       cache = lane < pr_g.np ? pair_entry(a, pr_pair, pr_g, lane) : Entry{-1, 0, 0, -1};
+      if (app_one) pr_row = load_single_row(a, pr_pair / a.Hkv, pr_pair % a.Hkv, lane);
     } else if (pr_e - pr_base >= 32) {
       pr_base = pr_e;
       cache = pr_base + lane < pr_g.np ? pair_entry(a, pr_pair, pr_g, pr_base + lane)
@@ -147,7 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ehi = __shfl_sync(0xffffffffu, cache.hi, li);
     const int phys = __shfl_sync(0xffffffffu, cache.phys, li);
     const int st = static_cast<int>(pr_k % kAttnStages);
-    append_rows_in_page(a, pr_pair / a.Hkv, pr_pair % a.Hkv, pr_g.L, lp, phys, lane);
+    if (app_one)
+      store_single_row(a, pr_pair % a.Hkv, pr_g.L, lp, phys, lane, pr_row);
+    else
+      append_rows_in_page<1>(a, pr_pair / a.Hkv, pr_pair % a.Hkv, pr_g.L, lp, phys, lane);
     if (lane == 0) {
       my_meta[2 * st] = make_int4(lp, elo, ehi, phys);
       my_meta[2 * st + 1] = make_int4(pr_pair, pr_e, pr_g.np, pr_g.L);
