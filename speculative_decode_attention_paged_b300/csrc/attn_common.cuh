@@ -186,29 +186,46 @@ __device__ void block_exclusive_scan(int* vals, int n, int* scratch) {
   __syncthreads();
 }
 
-// Normalised mass of one page: sum over rows r < R of 2^(lse_page[r] - LSE[r]).
-// lse_page is 16-byte aligned when R is a multiple of 4.
-__device__ __forceinline__ float page_mass_of(const float* lse_page, const float* row_lse, int R) {
-  float mass = 0.f;
-  if ((R & 3) == 0) {
-#pragma unroll 8
-    for (int r = 0; r < R; r += 4) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(lse_page + r));
-      const float e[4] = {v.x, v.y, v.z, v.w};
+// Normalised page mass of one pair: dst[lp] = sum over rows r < R of
+// 2^(lse[lp][r] - LSE[r]) for pages lp < np, zero for np <= lp < stride.
+// Thread t of nthreads takes pages t, t + nthreads, ...; it keeps the loads of
+// kU pages x 4 rows in flight (a page at a time left one dependent load chain
+// per page, which ran at the end of the kernel), and sums each page's rows in
+// the order r = 0, 1, ....
+template <int kU>
+__device__ __forceinline__ void write_pair_mass(float* dst, const float* lse, const float* row_lse, int R, int np,
+                                                int stride, int t, int nthreads) {
+  for (int lp0 = t; lp0 < stride; lp0 += nthreads * kU) {
+    float acc[kU];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float L = row_lse[r + k];
-        if (e[k] != kNegInf && L != kNegInf) mass += fast_exp2(e[k] - L);
+    for (int u = 0; u < kU; ++u) acc[u] = 0.f;
+    if (lp0 < np) {
+      for (int r0 = 0; r0 < R; r0 += 4) {
+        float v[kU][4];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int lp = lp0 + u * nthreads;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            v[u][k] = (lp < np && r0 + k < R) ? __ldcg(lse + static_cast<int64_t>(lp) * R + r0 + k) : kNegInf;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (r0 + k < R) {
+            const float L = row_lse[r0 + k];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+              if (v[u][k] != kNegInf && L != kNegInf) acc[u] += fast_exp2(v[u][k] - L);
+          }
+        }
       }
     }
-  } else {
-    for (int r = 0; r < R; ++r) {
-      const float v = __ldcg(lse_page + r);
-      const float L = row_lse[r];
-      if (v != kNegInf && L != kNegInf) mass += fast_exp2(v - L);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int lp = lp0 + u * nthreads;
+      if (lp < stride) dst[lp] = lp < np ? acc[u] : 0.f;
     }
   }
-  return mass;
 }
 
 // Zero output rows (and zero page mass) of a pair with no page to read.

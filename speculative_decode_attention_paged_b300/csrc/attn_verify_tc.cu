@@ -716,8 +716,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(kAllBar, kSoftmaxThreads);
         float* dst = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
         const float* plse = a.page_lse + static_cast<int64_t>(pair) * a.max_pages * a.R;
-        for (int lp = sm_tid; lp < a.mass_stride; lp += kSoftmaxThreads)
-          dst[lp] = lp < np ? page_mass_of(plse + static_cast<int64_t>(lp) * a.R, row_lse, a.R) : 0.f;
+        write_pair_mass<4>(dst, plse, row_lse, a.R, np, a.mass_stride, sm_tid, kSoftmaxThreads);
       }
       ++seg_index;
       named_bar_sync(kAllBar, kSoftmaxThreads);
