@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     float* dst = a.page_mass + static_cast<int64_t>(cur_pair) * a.mass_stride;
     const float* pl = a.page_lse + static_cast<int64_t>(cur_pair) * a.max_pages * a.R;
-    write_pair_mass<8>(dst, pl, my_lse, a.R, cur_np, a.mass_stride, lane, 32);
+    write_pair_mass<16>(dst, pl, my_lse, a.R, cur_np, a.mass_stride, lane, 32);
   };
 
   // Slot of segment j of a pair cut by warp shares: the pair's pages start at
