@@ -98,3 +98,38 @@ def test_new_entry_points_validate_on_host(lib):
     # length commit: negative sizes, missing workspace
     assert lib.s3r_commit_lengths(None, None, -1, 4, 100, None, None, 0, None) == 1
     assert lib.s3r_commit_lengths(None, None, 4, 4, 100, None, None, 0, None) == 4
+
+
+def test_fused_append_calls_validate_rows_on_host(lib):
+    """The *_attn_append calls reject a missing rows struct, a row count other
+    than the call's (1 for dense and draft, the verify block's T), missing row
+    pointers and rows that are not 16-byte aligned, before any device work.
+    The addresses below are never dereferenced: every case fails on the host."""
+    kv = _kv(num_seqs=2, k_pool=0x10000, v_pool=0x20000, block_table=0x30000)
+    lens, q, out, ws, sel, cnt = 0x40000, 0x50000, 0x60000, 0x100000, 0x70000, 0x80000
+    one = 1.0
+
+    def rows(n, k=0x90000, v=0xA0000):
+        return ctypes.byref(s3r._KVRows(k_rows=k, v_rows=v, n_rows=n))
+
+    def dense(r, w=ws):
+        return lib.s3r_dense_decode_attn_append(ctypes.byref(kv), lens, r, q, out, one, w, 1 << 30, None)
+
+    def draft(r, pos=0):
+        return lib.s3r_sparse_draft_attn_append(ctypes.byref(kv), lens, pos, sel, cnt, 4, r, q, out, one, ws,
+                                                1 << 30, None)
+
+    def verify(T, r):
+        return lib.s3r_verify_attn_append(ctypes.byref(kv), lens, T, r, q, out, None, 0, one, ws, 1 << 30, None)
+
+    assert dense(None) == 1
+    assert dense(rows(2)) == 1                   # one row per sequence
+    assert dense(rows(1, k=None)) == 1
+    assert dense(rows(1, v=0xA0008)) == 1        # not 16-byte aligned
+    assert dense(rows(1), w=None) == 4           # the workspace is checked first
+    assert draft(None) == 1
+    assert draft(rows(3)) == 1
+    assert draft(rows(1), pos=-1) == 1
+    assert verify(3, None) == 1
+    assert verify(3, rows(2)) == 1               # the block's T rows
+    assert verify(3, rows(3, k=0x90004)) == 1
