@@ -350,13 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Publish this segment; the last of the pair's segments to arrive merges.
       const int gwa = share_of(N, cur_start, tw);
       const int nseg = N >= tw ? share_of(N, cur_start + cur_np - 1, tw) - gwa + 1 : cur_np;
-      __threadfence();
+      fence_acq_rel_gpu();
       __syncwarp();
       int last = 0;
       if (lane == 0) last = atomicAdd(a.arrivals + cur_pair, 1) == nseg - 1;
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
-        __threadfence();
+        fence_acq_rel_gpu();
         merge_pair(nseg, gwa);
         if (MASS && a.page_mass != nullptr) write_mass();
         if (lane == 0) a.arrivals[cur_pair] = 0;   // ready for the next call

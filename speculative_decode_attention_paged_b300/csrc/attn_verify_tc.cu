@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (q4 == 0 && (lane & 1) == 0 && r0 + jr < a.R)
           *reinterpret_cast<float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + r0 + jr) * 2) =
               make_float2(m_jr, L_l);
-        __threadfence();
+        fence_acq_rel_gpu();
         named_bar_sync(kAllBar, kSoftmaxThreads);
         const int gwa = share_of(N, pstart, tw);
         const int nseg = N >= tw ? share_of(N, pstart + np - 1, tw) - gwa + 1 : np;
@@ -674,7 +674,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(kAllBar, kSoftmaxThreads);
         last = *last_flag;
         if (last) {
-          __threadfence();
+          fence_acq_rel_gpu();
           auto slot_of = [&](int j) -> int {
             if (N >= tw) return (gwa + j) * 2 + ((j == 0 && share_start(N, gwa, tw) < pstart) ? 1 : 0);
             return share_of(N, pstart + j, tw) * 2;

@@ -43,6 +43,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Release / acquire fence at GPU scope: a thread's writes before it are seen
+// by a thread of another CTA that observes a later write (here: an arrival
+// counter) and then fences itself.  Message passing between CTAs needs no
+// more than this; __threadfence() is a sequentially consistent fence.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Orders this thread's generic-proxy global writes before async-proxy (TMA)
 // accesses that follow it.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -523,12 +523,12 @@ __device__ __forceinline__ bool split_chunks_arrive(const float* __restrict__ x,
   if (lane == 0) dst[c] = s;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
+    fence_acq_rel_gpu();
     s_last = atomicAdd(counter, 1) == arrivals_expected - 1;
   }
   __syncthreads();
   const bool last = s_last != 0;
-  if (last) __threadfence();
+  if (last) fence_acq_rel_gpu();
   return last;
 }
 
