@@ -196,7 +196,9 @@ S3R_API s3r_status s3r_verify_attn(const s3r_paged_kv* kv, const int32_t* hist_l
  *
  *   rows.k_rows, rows.v_rows  bf16 [num_seqs][rows.n_rows][num_kv_heads][128],
  *                16-byte aligned
- *   dense decode: n_rows = 1, the row of position ctx_lens[s] - 1
+ *   dense decode: n_rows = 1, the row of position ctx_lens[s] - 1 (none for a
+ *                 sequence with ctx_lens[s] = 0: it reads nothing and writes
+ *                 nothing, and its output rows are zero)
  *   sparse draft: n_rows = 1, the row of position hist_lens[s] + draft_pos
  *   verify:       n_rows = the call's n_rows, rows of positions
  *                 hist_lens[s] .. hist_lens[s] + n_rows - 1
