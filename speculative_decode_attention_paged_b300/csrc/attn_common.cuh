@@ -246,9 +246,11 @@ __device__ void zero_pair(const AttnArgs& a, int pair) {
 // The call's appended rows that fall in logical page lp of pair (s, h), whose
 // physical page is phys: written into the pool by the whole warp (lanes 0-15
 // the K row, lanes 16-31 the V row, 16 bytes each), then ordered before the
-// TMA load of that page that this warp issues next.  A pair's page is read by
-// one warp only, so no other reader can see the page before the rows land.
-// The loads of up to kBatch rows are in flight before any of their stores.
+// TMA load of that page that this warp issues next.  Each entry of a pair's
+// page stream is read by one warp only, so no reader sees the page before the
+// rows land.  (A draft page that is both selected and the draft tail is two
+// entries: both writers store the same bytes.)  The loads of up to kBatch rows
+// are in flight before any of their stores.
 template <int kBatch>
 __device__ __forceinline__ void append_rows_in_page(const AttnArgs& a, int s, int h, int L, int lp, int phys,
                                                     int lane) {
@@ -277,7 +279,7 @@ __device__ __forceinline__ void append_rows_in_page(const AttnArgs& a, int s, in
 }
 
 // Lines of pair (s, h)'s appended rows (app_rows of them, 256 bytes each for K
-// and for V) into L2 when a warp starts on the pair, so the loads of
+// and for V) into L2 when the producers start on the pair, so the loads of
 // append_rows_in_page at the pair's tail page hit L2.
 __device__ __forceinline__ void prefetch_pair_rows(const AttnArgs& a, int s, int h, int lane) {
   for (int i = lane; i < a.app_rows * 4; i += 32) {
