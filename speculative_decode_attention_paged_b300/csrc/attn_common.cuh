@@ -228,6 +228,31 @@ __device__ __forceinline__ void write_pair_mass(float* dst, const float* lse, co
   }
 }
 
+// Normalised mass of one page: sum over rows r < R of 2^(lse_page[r] - LSE[r]).
+// lse_page is 16-byte aligned when R is a multiple of 4.
+__device__ __forceinline__ float page_mass_of(const float* lse_page, const float* row_lse, int R) {
+  float mass = 0.f;
+  if ((R & 3) == 0) {
+#pragma unroll 8
+    for (int r = 0; r < R; r += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(lse_page + r));
+      const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float L = row_lse[r + k];
+        if (e[k] != kNegInf && L != kNegInf) mass += fast_exp2(e[k] - L);
+      }
+    }
+  } else {
+    for (int r = 0; r < R; ++r) {
+      const float v = __ldcg(lse_page + r);
+      const float L = row_lse[r];
+      if (v != kNegInf && L != kNegInf) mass += fast_exp2(v - L);
+    }
+  }
+  return mass;
+}
+
 // Zero output rows (and zero page mass) of a pair with no page to read.
 __device__ void zero_pair(const AttnArgs& a, int pair) {
   const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
@@ -276,17 +301,6 @@ __device__ __forceinline__ void append_rows_in_page(const AttnArgs& a, int s, in
   }
   fence_proxy_async_global();
   __syncwarp();
-}
-
-// Lines of pair (s, h)'s appended rows (app_rows of them, 256 bytes each for K
-// and for V) into L2 when the producers start on the pair, so the loads of
-// append_rows_in_page at the pair's tail page hit L2.
-__device__ __forceinline__ void prefetch_pair_rows(const AttnArgs& a, int s, int h, int lane) {
-  for (int i = lane; i < a.app_rows * 4; i += 32) {
-    const int t = i >> 2;
-    const uint4* src = (i & 2) ? a.app_v : a.app_k;
-    prefetch_l2(src + ((static_cast<int64_t>(s) * a.app_rows + t) * a.Hkv + h) * 16 + (i & 1) * 8);
-  }
 }
 
 // The one appended row of pair (s, h) (calls with app_rows == 1), this lane's

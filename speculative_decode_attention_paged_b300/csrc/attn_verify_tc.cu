@@ -285,7 +285,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           e = 0;
           first_of_pair = true;
         }
-        if (first_of_pair && pid == 0 && a.app_rows > 0) prefetch_pair_rows(a, pair / a.Hkv, pair % a.Hkv, lane);
         const int64_t rest = x1 - x;
         const int n = min(kTcTilePages, min(g.np - e, rest < kTcTilePages ? static_cast<int>(rest) : kTcTilePages));
         const bool last = (e + n == g.np) || (x + n == x1);
@@ -295,25 +294,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           cbase = e;
           cache = cbase + lane < g.np ? pair_entry(a, pair, g, cbase + lane) : Entry{-1, 0, 0, -1};
         }
-        const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
-        const int src_lane = e - cbase + (lane & (kTcTilePages - 1));
-        Entry en;
-        en.lp = -1;
-        en.lo = __shfl_sync(0xffffffffu, cache.lo, src_lane);
-        en.hi = __shfl_sync(0xffffffffu, cache.hi, src_lane);
-        en.phys = __shfl_sync(0xffffffffu, cache.phys, src_lane);
-        // appended block rows of this tile's pages, each written by the producer
-        // warp that issues the page's boxes; they go to the pool, not to the
-        // stage, so they are written before waiting for the stage to drain
-        if (a.app_rows > 0 && (g.L + a.app_rows - 1) / kPage >= e && g.L / kPage < e + n) {
-          for (int p = pid; p < n; p += kTcProducers)
-            append_rows_in_page<8>(a, s, h, g.L, e + p, __shfl_sync(0xffffffffu, en.phys, p), lane);
-        }
         const int st = t % kTcStages;
         const uint32_t ph = static_cast<uint32_t>((t / kTcStages) & 1);
         int okw = 1;
         if (lane == 0) okw = wait_or_abort(&k_empty[st], ph ^ 1u, abort_flag, a.err);
         if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
+        const int s = pair / a.Hkv, h = pair - (pair / a.Hkv) * a.Hkv;
         if (first_of_pair && pid == 0) {
           if (lane == 0) okw = wait_or_abort(q_empty, static_cast<uint32_t>(q_uses & 1) ^ 1u, abort_flag, a.err);
           if (!__shfl_sync(0xffffffffu, okw, 0)) { ok = false; break; }
@@ -324,6 +310,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (first_of_pair) ++q_uses;
+        const int src_lane = e - cbase + (lane & (kTcTilePages - 1));
+        Entry en;
+        en.lp = -1;
+        en.lo = __shfl_sync(0xffffffffu, cache.lo, src_lane);
+        en.hi = __shfl_sync(0xffffffffu, cache.hi, src_lane);
+        en.phys = __shfl_sync(0xffffffffu, cache.phys, src_lane);
         const bool load = lane < n && en.phys >= 0;
         TileMeta& m = meta[t % kMetaSlots];
         if (pid == 0 && lane < kTcTilePages) {
@@ -346,6 +338,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&k_full[st], __popc(loadmask) * 2u * kHalfBytes);
         }
         __syncwarp();
+        // appended block rows of this tile's pages, each written by the producer
+        // warp that issues the page's boxes, before it issues them
+        if (a.app_rows > 0 && (g.L + a.app_rows - 1) / kPage >= e && g.L / kPage < e + n) {
+          for (int p = pid; p < n; p += kTcProducers)
+            append_rows_in_page<8>(a, s, h, g.L, e + p, __shfl_sync(0xffffffffu, en.phys, p), lane);
+        }
         const bool mine = load && (lane % kTcProducers) == pid;
         uint8_t* dst = stages + static_cast<size_t>(st) * kTcStageBytes + lane * kHalfBytes;
         const int y = h * kPage;
@@ -666,7 +664,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (q4 == 0 && (lane & 1) == 0 && r0 + jr < a.R)
           *reinterpret_cast<float2*>(a.part_ml + (static_cast<int64_t>(slot) * a.R + r0 + jr) * 2) =
               make_float2(m_jr, L_l);
-        fence_acq_rel_gpu();
+        __threadfence();
         named_bar_sync(kAllBar, kSoftmaxThreads);
         const int gwa = share_of(N, pstart, tw);
         const int nseg = N >= tw ? share_of(N, pstart + np - 1, tw) - gwa + 1 : np;
@@ -674,7 +672,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(kAllBar, kSoftmaxThreads);
         last = *last_flag;
         if (last) {
-          fence_acq_rel_gpu();
+          __threadfence();
           auto slot_of = [&](int j) -> int {
             if (N >= tw) return (gwa + j) * 2 + ((j == 0 && share_start(N, gwa, tw) < pstart) ? 1 : 0);
             return share_of(N, pstart + j, tw) * 2;
@@ -716,7 +714,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(kAllBar, kSoftmaxThreads);
         float* dst = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
         const float* plse = a.page_lse + static_cast<int64_t>(pair) * a.max_pages * a.R;
-        write_pair_mass<4>(dst, plse, row_lse, a.R, np, a.mass_stride, sm_tid, kSoftmaxThreads);
+        for (int lp = sm_tid; lp < a.mass_stride; lp += kSoftmaxThreads)
+          dst[lp] = lp < np ? page_mass_of(plse + static_cast<int64_t>(lp) * a.R, row_lse, a.R) : 0.f;
       }
       ++seg_index;
       named_bar_sync(kAllBar, kSoftmaxThreads);
