@@ -17,10 +17,10 @@ performance").  The rule itself is not printed, so this library fixes one:
         page index first
   emitted in ascending page order, count B.
 
-Parity status: parity unpinned with respect to the pages (they give no rule);
-the rule above is pinned by tests/test_oracle_select.py against brute force
-over all B-subsets on tiny inputs and its invariants (|sel| = B, M within sel,
-ascending, budget 1.0 -> all pages).
+Parity status: pinned by tests/test_oracle_select.py against brute force over
+all B-subsets on tiny inputs and by its invariants (|sel| = B, M within sel,
+ascending, budget 1.0 -> all pages).  The rule is a reading: the pages print
+none, so what is pinned is this rule, not a formula of theirs.
 """
 
 import math
