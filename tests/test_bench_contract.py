@@ -1,0 +1,56 @@
+"""The reference arm of bench.py prints the one-line JSON contract: the base
+keys, a cpu_baseline describing the run, and an e2e block with no host-device
+traffic.  The oracle sample is stubbed so the test checks the line, not the
+oracle's speed (a real sample takes about a minute of CPU time)."""
+
+import contextlib
+import io
+import json
+import types
+
+import bench
+
+
+def _stub_sample(calls):
+    def sample(seconds, seed=0):
+        calls.append(seconds)
+        return 2.0e9, 0.5, "stub: 2 GB of sequence passes in 0.5 s"
+    return sample
+
+
+def test_reference_line_keys_and_values(monkeypatch):
+    calls = []
+    monkeypatch.setattr(bench, "oracle_sample", _stub_sample(calls))
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        assert bench.main(["--impl", "reference", "--steps", "4", "--warmup", "3"]) == 0
+    lines = [ln for ln in out.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["steps"] == 4 and d["warmup"] == 3 and d["n_gpus"] == 1
+    # 4 timed samples of 2 GB in 0.5 s each: 4 GB/s, 500 ms per step
+    assert abs(d["value"] - 4.0) < 1e-12 and abs(d["ms_per_step"] - 500.0) < 1e-9
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["dtype"] == "f64" and d["data"] == "synthetic" and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == d["unit"]
+    assert isinstance(cb["cores"], int) and cb["cores"] >= 1 and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    # 3 warm-up samples then 4 timed ones, each bounded so the whole run stays near a minute
+    assert len(calls) == 7 and all(0 < s <= 60.0 for s in calls)
+
+
+def test_reference_other_ranks_print_nothing(monkeypatch):
+    calls = []
+    monkeypatch.setattr(bench, "oracle_sample", _stub_sample(calls))
+    args = types.SimpleNamespace(steps=2, warmup=3, gpus=2)
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        assert bench.run_reference(args, 2, 1) == 0
+    assert out.getvalue() == "" and calls == []
