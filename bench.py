@@ -468,13 +468,8 @@ def run_s3r(args, world, rank, local):
     dense_avg_bytes = sum(b["dense"]) / k
     dense_launch = statistics.mean(dense_launch_ms)
     achieved = dense_avg_bytes / (dense_launch * 1e-3) / 1e9
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
-    peak = float(peaks.get("hbm_gbs", 6400.0))
+    peaks = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     nacc = w.n_acc.cpu().numpy()
@@ -532,6 +527,21 @@ def run_s3r(args, world, rank, local):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+# Roofline denominators when MEASURED_PEAKS.json is absent: one earlier
+# measurement of a B300 (copy bandwidth; dense bf16 GEMM held for seconds).
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1400.0
+
+
+def measured_peaks(root=None):
+    """The measured peaks file at the repo root as a dict ({} if absent)."""
+    try:
+        with open(os.path.join(root or ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
 
 
 # (dram__bytes_read.sum + dram__bytes_write.sum) / algorithmic bytes of one
@@ -1096,13 +1106,9 @@ def run_scheduler(args):
     weight_bytes = 16.4e9
     page_bytes = kv_token_bytes * page_tokens
     pool = int(100e9 // page_bytes)
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        peaks = {}
-    hbm = float(peaks.get("hbm_gbs", 6400.0)) * 1e9
-    tflops = float(peaks.get("bf16_tflops_sustained", 1400.0)) * 1e12
+    peaks = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)) * 1e9
+    tflops = float(peaks.get("bf16_tflops_sustained", FALLBACK_BF16_TFLOPS_SUSTAINED)) * 1e12
     link = _host_link_gbs()
     link_src = "measured" if link is not None else "assumed"
     link = (link or 55.0) * 1e9

@@ -54,3 +54,13 @@ def test_reference_other_ranks_print_nothing(monkeypatch):
     with contextlib.redirect_stdout(out):
         assert bench.run_reference(args, 2, 1) == 0
     assert out.getvalue() == "" and calls == []
+
+
+def test_measured_peaks_file_and_fallback(tmp_path):
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6492.7, "bf16_tflops": 1810.1}))
+    assert bench.measured_peaks(str(tmp_path))["hbm_gbs"] == 6492.7
+    empty = tmp_path / "none"
+    empty.mkdir()
+    assert bench.measured_peaks(str(empty)) == {}
+    # the fallback figures are the ones the roofline uses without the file
+    assert bench.FALLBACK_HBM_GBS == 6400.0 and bench.FALLBACK_BF16_TFLOPS_SUSTAINED == 1400.0
