@@ -1,7 +1,6 @@
 """Data-dependent errors never fault: the kernels skip the bad item, finish,
 and set a bit in the workspace's error word (read on the host)."""
 
-import numpy as np
 import pytest
 import torch
 

@@ -1,7 +1,6 @@
 """GPU parity of draft-page selection: bit-exact against the oracle rule when
 both read the same fp32 page mass (including exact ties), plus edge cases."""
 
-import math
 
 import numpy as np
 import pytest

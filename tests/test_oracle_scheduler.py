@@ -6,7 +6,6 @@ decisions."""
 
 import math
 
-import numpy as np
 import pytest
 
 from oracle.scheduler import (POLICY_AIMD, POLICY_FIXED_OFFLOAD, POLICY_RECOMPUTE, simulate)

@@ -7,7 +7,7 @@ with comparable task performance"), the budget sweep 0.05 .. 0.50 ([rebas]
 "为什么值得关注").  The data are synthetic: no model weights or datasets.
 """
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 from typing import Optional, Tuple
 
 
