@@ -206,9 +206,9 @@ S3R_API s3r_status s3r_verify_attn(const s3r_paged_kv* kv, const int32_t* hist_l
  * read: the call reports S3R_DEVERR_BAD_PAGE).  The pages that receive rows
  * must not be shared with another sequence of the call.  The pool descriptor's
  * k_pool and v_pool are written; the rows are caller-owned device memory, read
- * only.  Before anything is enqueued, a missing rows struct, rows.n_rows other
- * than stated above, or a null or unaligned row pointer returns
- * S3R_ERR_INVALID_ARG (after the plain call's own checks).
+ * only.  A missing rows struct returns S3R_ERR_INVALID_ARG at once; after the
+ * plain call's own checks, so do rows.n_rows other than stated above and a
+ * null or unaligned row pointer.  Nothing is enqueued in either case.
  */
 typedef struct s3r_kv_rows {
   const void* k_rows;
