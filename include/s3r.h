@@ -267,6 +267,16 @@ S3R_API s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t*
  *   out_tokens   int32 [n][k+1] out: accepted drafts, then the correcting or
  *                bonus token, then -1
  *   n_accepted   int32 [n] out
+ *   tie_count    optional (NULL to skip) uint32 [2] out, zeroed by the call:
+ *                [0] the ratio tests, up to and including each sequence's
+ *                first rejection, whose uniform lies within 1e-6 of the
+ *                ratio (|u - p_i(x_i)/q_i(x_i)| <= 1e-6); [1] the sequences
+ *                whose inverse-CDF target u*Z lies within 1e-6*Z of either end
+ *                of the picked token's interval of the running sum (or that
+ *                took the rounding fallback).  These are the decisions that
+ *                rounding in the fp32 row statistics could flip against an
+ *                exact evaluation; the tokens stay valid samples, and the
+ *                counts say how many such decisions a call made.
  * With p_i = softmax(p_logits[i]), q_i = softmax(q_logits[i]) (temperature 1),
  * draft x_i is accepted iff u < p_i(x_i) / q_i(x_i), u = Philox4x32-10 uniform
  * of counter (n, i-1, 0, offset) and key seed; at the first rejection the
@@ -278,7 +288,8 @@ S3R_API s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t*
 S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
                            const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
                            uint64_t seed, uint64_t offset, int32_t* out_tokens,
-                           int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
+                           int32_t* n_accepted, uint32_t* tie_count, void* ws, size_t ws_bytes,
+                           void* stream);
 
 /*
  * Exact speculative sampling with the ratio tests taken one draft position at
@@ -289,8 +300,9 @@ S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
  * rebasdaily.com, "草稿可以稀疏，交卷必须完整"), so the skipped rows cannot
  * change the result.
  *
- * Same arguments, semantics, results (bit for bit) and workspace size as
- * s3r_spec_sample.  It enqueues k + 3 kernels instead of 4 and reads about
+ * Same arguments, semantics, results (bit for bit, tie counts included) and
+ * workspace size as s3r_spec_sample.  It enqueues k + 3 kernels instead of 4
+ * (plus a clear of tie_count when given) and reads about
  * (2 E[a] + 2) / (2k + 1) of the logit bytes, E[a] the mean accepted count.
  * Its workspace must hold zeroed arrival counters (s3r_workspace_init once
  * after allocation); every call leaves them at zero.
@@ -298,7 +310,8 @@ S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
 S3R_API s3r_status s3r_spec_sample_sequential(const float* p_logits, const float* q_logits,
                                       const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
                                       uint64_t seed, uint64_t offset, int32_t* out_tokens,
-                                      int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
+                                      int32_t* n_accepted, uint32_t* tie_count, void* ws, size_t ws_bytes,
+                                      void* stream);
 
 /* Workspace bytes for s3r_sample_draft_tokens with n sequences (host). */
 S3R_API s3r_status s3r_sample_draft_workspace_size(int32_t n, size_t* bytes);
@@ -378,20 +391,25 @@ S3R_API s3r_status s3r_commit_lengths(const int32_t* hist_lens, const int32_t* n
  * are serving.  The S³R pages have no counterpart to this call; it exists
  * only for such callers.
  *
- * Same arguments, semantics and results as s3r_spec_sample, without ws and
- * ws_bytes.  Its scratch is a fixed S3R_NOALLOC_SCRATCH_BYTES array in the
- * library's device image, so it never calls cudaMalloc, cudaFree or any
- * allocating routine.
+ * Same arguments, semantics and results as s3r_spec_sample, without
+ * tie_count, ws and ws_bytes.  Its scratch is a fixed
+ * S3R_NOALLOC_SCRATCH_BYTES array in the library's device image, so it never
+ * calls cudaMalloc, cudaFree or any allocating routine.
  *   device_error  optional (NULL to skip) device int32 that receives this
  *                 call's device error bits (the S3R_DEVERR_* values)
  * Returns S3R_ERR_UNSUPPORTED, before enqueuing anything, when
  * s3r_spec_sample_workspace_size(n, k) exceeds S3R_NOALLOC_SCRATCH_BYTES
- * (for example n = 2048 with k = 8 needs 1,868,032 bytes and fits).
- * The first call on each device looks up the array's device address (a
- * one-time set-up per device, with that device current): make that first
- * call before any stream capture.  Every call on a device shares the one
- * array and overwrites it, so calls whose work may overlap on the GPU
- * (different streams without ordering) race and must not be issued.
+ * (for example n = 2048 with k = 8 needs 1,868,032 bytes and fits).  Every
+ * other argument error also returns before anything is enqueued.
+ * The stream and every pointer must belong to the CURRENT device: the call
+ * uses the current device's copy of the array.  The first call on each
+ * device looks up the array's device address (a one-time set-up per device,
+ * with that device current): make that first call before any stream capture.
+ * A call that fails with S3R_ERR_CUDA drops the cached address, and the next
+ * call looks it up again; a device reset (cudaDeviceReset) between calls is
+ * not otherwise supported.  Every call on a device shares the one array and
+ * overwrites it, so calls whose work may overlap on the GPU (different
+ * streams without ordering) race and must not be issued.
  */
 S3R_API s3r_status s3r_spec_sample_noalloc(const float* p_logits, const float* q_logits,
                                    const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,

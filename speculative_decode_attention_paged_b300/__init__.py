@@ -106,9 +106,9 @@ _SIG = {
     "s3r_select_draft_pages": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, ctypes.c_double, _I32, _I32, _P, _P,
                                               _I32, _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64, _P, _P,
-                                       _P, ctypes.c_size_t, _P]),
+                                       _P, _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample_sequential": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
-                                                  _P, _P, _P, ctypes.c_size_t, _P]),
+                                                  _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "s3r_spec_sample_noalloc": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, ctypes.c_uint64, ctypes.c_uint64,
                                                _P, _P, _P, _P]),
     "s3r_sample_draft_workspace_size": (ctypes.c_int, [_I32, ctypes.POINTER(ctypes.c_size_t)]),
@@ -165,16 +165,46 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _need(t, dtype, name):
+def _on_current_device(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
+
+
+def _need(t, dtype, name, shape=None):
+    """A contiguous CUDA tensor of `dtype` on the current device; `shape`, when
+    given, is the exact shape it must have."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t
+
+
+def _need_at_least(t, dtype, name, numel):
+    _need(t, dtype, name)
+    if t.numel() < numel:
+        raise ValueError(f"{name} must hold at least {numel} elements")
+    return t
+
+
+def _spec_args(p_logits, q_logits, draft_tokens, out_tokens, n_accepted):
+    """Checks every sampler tensor against p_logits' (n, k + 1, vocab)."""
+    _need(p_logits, torch.float32, "p_logits")
+    if p_logits.dim() != 3 or p_logits.shape[1] < 1:
+        raise ValueError("p_logits must be [n][k+1][vocab]")
+    n, k1, V = p_logits.shape
+    _need(q_logits, torch.float32, "q_logits", (n, k1 - 1, V))
+    _need(draft_tokens, torch.int32, "draft_tokens", (n, k1 - 1))
+    _need(out_tokens, torch.int32, "out_tokens", (n, k1))
+    _need(n_accepted, torch.int32, "n_accepted", (n,))
+    return n, k1 - 1, V
 
 
 class PagedKVDesc:
@@ -339,32 +369,29 @@ def s3r_select_draft_pages(page_mass, sel_lens, budget, sel_pages, sel_count, ws
 
 
 def s3r_spec_sample(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, n_accepted, ws: Workspace,
-                    stream=None):
-    _need(p_logits, torch.float32, "p_logits")
-    _need(q_logits, torch.float32, "q_logits")
-    _need(draft_tokens, torch.int32, "draft_tokens")
-    _need(out_tokens, torch.int32, "out_tokens")
-    _need(n_accepted, torch.int32, "n_accepted")
-    n, k1, V = p_logits.shape
-    _call("s3r_spec_sample", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1), _I32(V),
-          ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), ws.ptr(),
-          ctypes.c_size_t(ws.nbytes), _stream(stream))
+                    stream=None, tie_count=None):
+    """Exact speculative sampling.  tie_count: optional int32 CUDA tensor of
+    two elements that receives [ratio ties, inverse-CDF ties] (the C side's
+    uint32 counters; the counts stay far below 2^31)."""
+    n, k, V = _spec_args(p_logits, q_logits, draft_tokens, out_tokens, n_accepted)
+    if tie_count is not None:
+        _need_at_least(tie_count, torch.int32, "tie_count", 2)
+    _call("s3r_spec_sample", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k), _I32(V),
+          ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), _ptr(tie_count),
+          ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
     return out_tokens, n_accepted
 
 
 def s3r_spec_sample_sequential(p_logits, q_logits, draft_tokens, seed, offset, out_tokens, n_accepted,
-                               ws: Workspace, stream=None):
+                               ws: Workspace, stream=None, tie_count=None):
     """s3r_spec_sample with the ratio tests one position at a time, reading no
     row after a sequence's first rejection; the same results bit for bit."""
-    _need(p_logits, torch.float32, "p_logits")
-    _need(q_logits, torch.float32, "q_logits")
-    _need(draft_tokens, torch.int32, "draft_tokens")
-    _need(out_tokens, torch.int32, "out_tokens")
-    _need(n_accepted, torch.int32, "n_accepted")
-    n, k1, V = p_logits.shape
-    _call("s3r_spec_sample_sequential", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1),
-          _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted), ws.ptr(),
-          ctypes.c_size_t(ws.nbytes), _stream(stream))
+    n, k, V = _spec_args(p_logits, q_logits, draft_tokens, out_tokens, n_accepted)
+    if tie_count is not None:
+        _need_at_least(tie_count, torch.int32, "tie_count", 2)
+    _call("s3r_spec_sample_sequential", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k),
+          _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted),
+          _ptr(tie_count), ws.ptr(), ctypes.c_size_t(ws.nbytes), _stream(stream))
     return out_tokens, n_accepted
 
 
@@ -376,16 +403,12 @@ def s3r_spec_sample_noalloc(p_logits, q_logits, draft_tokens, seed, offset, out_
     """s3r_spec_sample without a workspace, for callers that cannot allocate
     device memory; the scratch lives in the library (see include/s3r.h).
     device_error: optional int32 CUDA tensor of one element that receives the
-    call's device error bits."""
-    _need(p_logits, torch.float32, "p_logits")
-    _need(q_logits, torch.float32, "q_logits")
-    _need(draft_tokens, torch.int32, "draft_tokens")
-    _need(out_tokens, torch.int32, "out_tokens")
-    _need(n_accepted, torch.int32, "n_accepted")
+    call's device error bits.  Every tensor must be on the current device,
+    whose copy of the library's scratch the call uses."""
+    n, k, V = _spec_args(p_logits, q_logits, draft_tokens, out_tokens, n_accepted)
     if device_error is not None:
-        _need(device_error, torch.int32, "device_error")
-    n, k1, V = p_logits.shape
-    _call("s3r_spec_sample_noalloc", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k1 - 1),
+        _need_at_least(device_error, torch.int32, "device_error", 1)
+    _call("s3r_spec_sample_noalloc", _ptr(p_logits), _ptr(q_logits), _ptr(draft_tokens), _I32(n), _I32(k),
           _I32(V), ctypes.c_uint64(seed), ctypes.c_uint64(offset), _ptr(out_tokens), _ptr(n_accepted),
           _ptr(device_error), _stream(stream))
     return out_tokens, n_accepted
@@ -404,8 +427,7 @@ def _need_rows(t, dtype, name, dims):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    _on_current_device(t, name)
     if t.dim() != dims or (dims > 1 and t.stride(-1) != 1):
         raise ValueError(f"{name} must be {dims}-D with a contiguous last dimension")
     return t

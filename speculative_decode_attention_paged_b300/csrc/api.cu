@@ -13,6 +13,21 @@
 #include "kv_append.cuh"
 
 namespace s3r {
+
+s3r_status check_spec_sample_args(const float* p_logits, const float* q_logits, const int32_t* draft_tokens,
+                                  int32_t n, int32_t k, int32_t vocab, uint64_t offset, const int32_t* out_tokens,
+                                  const int32_t* n_accepted) {
+  if (n < 0 || k < 0 || vocab <= 0) return S3R_ERR_INVALID_ARG;
+  if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
+  if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n) * (k + 1) * vocab > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(n) * std::max(2 * k + 1, kSampleChunks) > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
+  if (n == 0) return S3R_OK;
+  if (p_logits == nullptr || out_tokens == nullptr || n_accepted == nullptr) return S3R_ERR_INVALID_ARG;
+  if (k > 0 && (q_logits == nullptr || draft_tokens == nullptr)) return S3R_ERR_INVALID_ARG;
+  return S3R_OK;
+}
+
 cudaError_t launch_select_pages(const float* mass, const int32_t* sel_lens, int S, int Hkv,
                                 int stride, double budget, int n_sink, int n_recent,
                                 int32_t* sel_pages, int32_t* sel_count, int b_max, int* err,
@@ -24,7 +39,6 @@ namespace {
 using namespace s3r;
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxSpecK = 64;
 constexpr uint32_t kStreamDraftU = 2;   // Philox stream of draft-token sampling
 // Longest mass row the selection kernel stages in shared memory (pages).
 constexpr int kMaxSelectPages = 49152;
@@ -363,42 +377,50 @@ s3r_status s3r_select_draft_pages(const float* page_mass, const int32_t* sel_len
 static s3r_status check_spec_sample(const float* p_logits, const float* q_logits, const int32_t* draft_tokens,
                                      int32_t n, int32_t k, int32_t vocab, uint64_t offset, int32_t* out_tokens,
                                      int32_t* n_accepted, void* ws, size_t ws_bytes) {
-  if (n < 0 || k < 0 || vocab <= 0) return S3R_ERR_INVALID_ARG;
-  if (k > kMaxSpecK) return S3R_ERR_UNSUPPORTED;
-  if (offset > 0xffffffffULL) return S3R_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(n) * (k + 1) * vocab > (int64_t{1} << 40)) return S3R_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(n) * std::max(2 * k + 1, kSampleChunks) > 0x7fffffffLL) return S3R_ERR_UNSUPPORTED;
+  const s3r_status st =
+      s3r::check_spec_sample_args(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens, n_accepted);
+  if (st != S3R_OK) return st;
   size_t need = 0;
   s3r_spec_sample_workspace_size(n, k, &need);
   if (ws == nullptr || !aligned256(ws) || ws_bytes < need) return S3R_ERR_WORKSPACE;
-  if (n == 0) return S3R_OK;
-  if (p_logits == nullptr || out_tokens == nullptr || n_accepted == nullptr) return S3R_ERR_INVALID_ARG;
-  if (k > 0 && (q_logits == nullptr || draft_tokens == nullptr)) return S3R_ERR_INVALID_ARG;
   return S3R_OK;
+}
+
+// Zero the optional tie counters before the sampler kernels add to them.
+static s3r_status zero_ties(uint32_t* tie_count, cudaStream_t stream) {
+  if (tie_count == nullptr) return S3R_OK;
+  return to_status(cudaMemsetAsync(tie_count, 0, 2 * sizeof(uint32_t), stream));
 }
 
 s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
                            const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
                            uint64_t seed, uint64_t offset, int32_t* out_tokens,
-                           int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
-  const s3r_status st = check_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens,
-                                          n_accepted, ws, ws_bytes);
+                           int32_t* n_accepted, uint32_t* tie_count, void* ws, size_t ws_bytes, void* stream) {
+  s3r_status st = check_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens,
+                                    n_accepted, ws, ws_bytes);
+  if (st != S3R_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = zero_ties(tie_count, s);
   if (st != S3R_OK || n == 0) return st;
   return to_status(launch_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
-                                      static_cast<uint32_t>(offset), ws, out_tokens, n_accepted,
-                                      static_cast<cudaStream_t>(stream)));
+                                      static_cast<uint32_t>(offset), ws, out_tokens, n_accepted, s, 1, -1, 0, 1,
+                                      tie_count));
 }
 
 s3r_status s3r_spec_sample_sequential(const float* p_logits, const float* q_logits,
                                       const int32_t* draft_tokens, int32_t n, int32_t k, int32_t vocab,
                                       uint64_t seed, uint64_t offset, int32_t* out_tokens,
-                                      int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
-  const s3r_status st = check_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens,
-                                          n_accepted, ws, ws_bytes);
+                                      int32_t* n_accepted, uint32_t* tie_count, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  s3r_status st = check_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, offset, out_tokens,
+                                    n_accepted, ws, ws_bytes);
+  if (st != S3R_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = zero_ties(tie_count, s);
   if (st != S3R_OK || n == 0) return st;
   return to_status(launch_spec_sample_sequential(p_logits, q_logits, draft_tokens, n, k, vocab, seed,
-                                                 static_cast<uint32_t>(offset), ws, out_tokens, n_accepted,
-                                                 static_cast<cudaStream_t>(stream)));
+                                                 static_cast<uint32_t>(offset), ws, out_tokens, n_accepted, s,
+                                                 tie_count));
 }
 
 s3r_status s3r_sample_draft_tokens(const float* logits, int32_t n, int32_t vocab, int64_t row_stride,

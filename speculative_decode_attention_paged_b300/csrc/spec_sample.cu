@@ -43,6 +43,11 @@ namespace {
 
 constexpr int kStatThreads = 256;
 constexpr double kLog2eD = 1.4426950408889634074;
+// Tie windows of the optional tie counters: a ratio test with |u - p/q| at
+// most kRatioTie, and an inverse-CDF pick whose target u * Z lies within
+// kCdfTie * Z of an end of the chosen token's CDF interval.
+constexpr double kRatioTie = 1e-6;
+constexpr double kCdfTie = 1e-6;
 
 // 2^((x - m) log2 e) with m pre-scaled: mlog2 = m * log2 e.
 __device__ __forceinline__ float scaled_exp(float x, float mlog2) {
@@ -221,46 +226,66 @@ __device__ __forceinline__ SampleRow sample_row(const float* p, const float* q, 
   return row;
 }
 
-// The ratio test of one drafted token x: rejected unless u < p(x) / q(x), the
-// ratio formed in fp64 from the fp32 logits p(x), q(x) and the rows' (max, sum).
-__device__ __forceinline__ bool ratio_rejects(float lp, float lq, float2 sp, float2 sq, float u) {
+// p(x) / q(x) of one drafted token x, formed in fp64 from the fp32 logits
+// p(x), q(x) and the rows' (max, sum).
+__device__ __forceinline__ double draft_ratio(float lp, float lq, float2 sp, float2 sq) {
   const double e = (static_cast<double>(lp) - sp.x) - (static_cast<double>(lq) - sq.x);
-  const double ratio = exp2(e * kLog2eD) * static_cast<double>(sq.y) / static_cast<double>(sp.y);
-  return !(static_cast<double>(u) < ratio);
+  return exp2(e * kLog2eD) * static_cast<double>(sq.y) / static_cast<double>(sp.y);
+}
+
+// The ratio test: x is rejected unless u < p(x) / q(x).
+__device__ __forceinline__ bool ratio_rejects(double ratio, float u) { return !(static_cast<double>(u) < ratio); }
+
+// A ratio test whose uniform lies within kRatioTie of the ratio: a decision
+// that rounding in the row statistics could flip.
+__device__ __forceinline__ bool ratio_tie(double ratio, float u) {
+  return fabs(static_cast<double>(u) - ratio) <= kRatioTie;
 }
 
 // One warp per sequence: the k ratio tests.  Draft x_i is accepted iff
 // u(n, i-1, ACCEPT) < p_i(x_i) / q_i(x_i); the ratio is formed in fp64 from the
 // fp32 logits and row statistics.  Writes a = index of the first rejection
-// (k if none), the accepted drafts and the -1 padding after position a.
+// (k if none), the accepted drafts and the -1 padding after position a.  With
+// ties != null, ties[0] gains the number of tests up to and including the
+// first rejection whose uniform lies within kRatioTie of the ratio.
 __global__ void __launch_bounds__(256)
     accept_kernel(const float* __restrict__ p, const float* __restrict__ q,
                   const int32_t* __restrict__ drafts, int N, int k, int V, uint64_t seed,
                   uint32_t offset, const float2* __restrict__ stats, int32_t* __restrict__ accept,
-                  int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err) {
+                  int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err,
+                  uint32_t* __restrict__ ties) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (n >= N) return;
   const int np_rows = N * (k + 1);
   int first = k;
+  uint64_t tie_bits = 0;   // bit i: test i is a tie (k <= 64)
   for (int base = 0; base < k; base += 32) {
     const int i = base + lane;
-    bool rej = false;
+    bool rej = false, tie = false;
     if (i < k) {
       const int x = __ldg(drafts + static_cast<int64_t>(n) * k + i);
       if (x < 0 || x >= V) {
         report_error(err, S3R_DEVERR_BAD_TOKEN);
         rej = true;
       } else {
-        rej = ratio_rejects(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x),
-                            __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x),
-                            stats[static_cast<int64_t>(n) * (k + 1) + i],
-                            stats[np_rows + static_cast<int64_t>(n) * k + i],
-                            philox_uniform(seed, offset, n, i, kStreamAccept));
+        const double ratio = draft_ratio(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x),
+                                         __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x),
+                                         stats[static_cast<int64_t>(n) * (k + 1) + i],
+                                         stats[np_rows + static_cast<int64_t>(n) * k + i]);
+        const float u = philox_uniform(seed, offset, n, i, kStreamAccept);
+        rej = ratio_rejects(ratio, u);
+        tie = ratio_tie(ratio, u);
       }
     }
     const unsigned b = __ballot_sync(0xffffffffu, rej);
+    tie_bits |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, tie)) << base;
     if (b != 0u && first == k) first = base + __ffs(b) - 1;
+  }
+  if (ties != nullptr && lane == 0) {
+    const uint64_t upto = first >= 63 ? ~uint64_t{0} : ((uint64_t{1} << (first + 1)) - 1);
+    const int c = __popcll(tie_bits & upto);
+    if (c > 0) atomicAdd(ties, static_cast<uint32_t>(c));
   }
   int32_t* out = out_tokens + static_cast<int64_t>(n) * (k + 1);
   for (int i = lane; i <= k; i += 32) {
@@ -357,15 +382,16 @@ __global__ void __launch_bounds__(kStatThreads)
 // Warp-wide, lane c holding chunk c's mass v >= 0 (fp64): the chunk where the
 // inverse CDF of u lands -- the first whose inclusive prefix (token order)
 // exceeds u * Z, Z the last prefix; the last chunk with mass if rounding puts
-// none past it; chunk 0 if every mass is 0 -- and the target's offset into it.
-__device__ __forceinline__ void choose_chunk(double v, double u, int lane, int& chunk, double& tgt) {
+// none past it; chunk 0 if every mass is 0 -- the target's offset into it, and Z.
+__device__ __forceinline__ void choose_chunk(double v, double u, int lane, int& chunk, double& tgt, double& total) {
   double incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const double t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
-  const double target = u * __shfl_sync(0xffffffffu, incl, 31);
+  total = __shfl_sync(0xffffffffu, incl, 31);
+  const double target = u * total;
   const unsigned over = __ballot_sync(0xffffffffu, incl > target);
   const unsigned pos = __ballot_sync(0xffffffffu, v > 0.0);
   chunk = over != 0u ? __ffs(over) - 1 : (pos != 0u ? 31 - __clz(pos) : 0);
@@ -378,7 +404,7 @@ static_assert(kPickThreads == kStatThreads, "the bonus sampler runs both phases 
 
 struct PickSmem {
   double warp_tot[kPickThreads / 32];
-  int owner, last, pick;
+  int owner, last, pick, tie;
 };
 
 // Block-wide inverse CDF inside chunk [lo, hi) of `row`: the first token whose
@@ -389,15 +415,18 @@ struct PickSmem {
 // (the same values, now from L1).  When rounding leaves the target past that
 // run, the run's last token with mass is taken, else the chunk's.  Nothing is
 // staged in shared memory, so kernels that stream rows before picking keep
-// their L1 for loads in flight.  Every thread returns the token.
+// their L1 for loads in flight.  Every thread returns the token.  sm.tie is
+// set when the target lies within eps of either end of the picked token's
+// interval of the running sum (or a rounding fallback picked it).
 __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo, int hi, double tgt,
-                                                   PickSmem& sm) {
+                                                   double eps, PickSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int len = hi - lo;
   if (tid == 0) {
     sm.owner = -1;
     sm.last = -1;
     sm.pick = -1;
+    sm.tie = 0;
   }
   const int E = (len + kPickThreads - 1) / kPickThreads;
   const int r0 = min(lo + tid * E, hi), r1 = min(r0 + E, hi);
@@ -437,15 +466,19 @@ __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo,
     const double rem = tgt - excl;
     float run = 0.f;
     int pick = -1;
+    bool tie = true;   // a rounding fallback is a boundary case
     for (int v = r0; v < r1; ++v) {
       const float r = row.at(v);
+      const float before = run;
       run += r;
       if (r > 0.f && static_cast<double>(run) > rem) {
         pick = v;
+        tie = static_cast<double>(run) - rem <= eps || rem - static_cast<double>(before) <= eps;
         break;
       }
     }
     sm.pick = pick >= 0 ? pick : my_last;
+    sm.tie = tie ? 1 : 0;
   }
   __syncthreads();
   const int tok = sm.pick >= 0 ? sm.pick : (sm.last >= 0 ? sm.last : lo);
@@ -460,10 +493,11 @@ __global__ void __launch_bounds__(kPickThreads)
     pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
                 uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
                 const float2* __restrict__ bonus_chunks, const int32_t* __restrict__ accept,
-                const double2* __restrict__ chunk_sums, int32_t* __restrict__ out_tokens) {
+                const double2* __restrict__ chunk_sums, int32_t* __restrict__ out_tokens,
+                uint32_t* __restrict__ ties) {
   __shared__ PickSmem sm;
   __shared__ int s_chunk, s_use_p;
-  __shared__ double s_tgt;
+  __shared__ double s_tgt, s_eps;
   const int n = blockIdx.x;
   const int tid = threadIdx.x;
   const int a = __ldg(accept + n);
@@ -485,20 +519,24 @@ __global__ void __launch_bounds__(kPickThreads)
     // the uniform of counter (n, a, RESAMPLE, offset)
     const double u = static_cast<double>(philox_uniform(seed, offset, n, a, kStreamResample));
     int chunk;
-    double tgt;
-    choose_chunk(v, u, tid, chunk, tgt);
+    double tgt, total;
+    choose_chunk(v, u, tid, chunk, tgt, total);
     if (tid == 0) {
       s_chunk = chunk;
       s_use_p = use_p ? 1 : 0;
       s_tgt = tgt;
+      s_eps = kCdfTie * total;
     }
   }
   __syncthreads();
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, s_use_p != 0);
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
-  const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, sm);
-  if (tid == 0) out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
+  const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, s_eps, sm);
+  if (tid == 0) {
+    out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
+    if (ties != nullptr && sm.tie) atomicAdd(ties + 1, 1u);
+  }
 }
 
 // Rows split over CTAs: each of kRowParts CTAs streams 8 chunks of a row (one
@@ -542,11 +580,11 @@ __global__ void __launch_bounds__(kStatThreads)
     bonus_sample_kernel(const float* __restrict__ p, int V, int64_t row_stride, uint64_t seed, uint32_t offset,
                         uint32_t u_stream, int u_pos, float2* __restrict__ chunks, int* __restrict__ arrivals,
                         int32_t* __restrict__ out_tokens, int64_t token_stride,
-                        int32_t* __restrict__ n_accepted) {
+                        int32_t* __restrict__ n_accepted, uint32_t* __restrict__ ties) {
   __shared__ PickSmem sm;
   __shared__ float2 s_row;
   __shared__ int s_chunk;
-  __shared__ double s_tgt;
+  __shared__ double s_tgt, s_eps;
   const int n = blockIdx.x / kRowParts;
   const int part = blockIdx.x - n * kRowParts;
   const int tid = threadIdx.x;
@@ -560,11 +598,12 @@ __global__ void __launch_bounds__(kStatThreads)
     r.y = __shfl_sync(0xffffffffu, r.y, 0);
     const double u = static_cast<double>(philox_uniform(seed, offset, n, u_pos, u_stream));
     int chunk;
-    double tgt;
-    choose_chunk(chunk_mass(cs, r), u, tid, chunk, tgt);
+    double tgt, total;
+    choose_chunk(chunk_mass(cs, r), u, tid, chunk, tgt, total);
     if (tid == 0) {
       s_chunk = chunk;
       s_tgt = tgt;
+      s_eps = kCdfTie * total;
       s_row = r;
       arrivals[n] = 0;
       n_accepted[n] = 0;
@@ -580,8 +619,11 @@ __global__ void __launch_bounds__(kStatThreads)
   row.izq = 0.f;
   const int CL = chunk_len(V);
   const int lo = min(s_chunk * CL, V), hi = min(lo + CL, V);
-  const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, sm);
-  if (tid == 0) out_tokens[static_cast<int64_t>(n) * token_stride] = tok;
+  const int tok = block_pick_in_chunk(row, lo, hi, s_tgt, s_eps, sm);
+  if (tid == 0) {
+    out_tokens[static_cast<int64_t>(n) * token_stride] = tok;
+    if (ties != nullptr && sm.tie) atomicAdd(ties + 1, 1u);
+  }
 }
 
 // Step i of the sequential (early-exit) ratio tests.  For i < k the rows p_i
@@ -599,7 +641,8 @@ __global__ void __launch_bounds__(kStatThreads)
                     const int32_t* __restrict__ drafts, int N, int k, int V, int i, uint64_t seed,
                     uint32_t offset, float2* __restrict__ stats, float2* __restrict__ pchunks,
                     float2* __restrict__ qchunks, int32_t* accept, int* __restrict__ arrivals,
-                    int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err) {
+                    int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err,
+                    uint32_t* __restrict__ ties) {
   const int rows = i < k ? 2 : 1;
   const int per_seq = rows * kRowParts;
   const int n = blockIdx.x / per_seq;
@@ -628,9 +671,11 @@ __global__ void __launch_bounds__(kStatThreads)
       if (x_i < 0 || x_i >= V) {
         report_error(err, S3R_DEVERR_BAD_TOKEN);
       } else {
-        rej = ratio_rejects(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x_i),
-                            __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x_i), rp, rq,
-                            philox_uniform(seed, offset, n, i, kStreamAccept));
+        const double ratio = draft_ratio(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x_i),
+                                         __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x_i), rp, rq);
+        const float u = philox_uniform(seed, offset, n, i, kStreamAccept);
+        rej = ratio_rejects(ratio, u);
+        if (ties != nullptr && ratio_tie(ratio, u)) atomicAdd(ties, 1u);
       }
       first = rej ? i : k;
       accept[n] = first;
@@ -651,7 +696,7 @@ __global__ void __launch_bounds__(kStatThreads)
 cudaError_t launch_residual_pick(const float* p, const float* q, int N, int k, int V, uint64_t seed,
                                  uint32_t offset, const float2* stats, const float2* bonus,
                                  const int32_t* accept, double2* chunks, int32_t* out_tokens, bool vec,
-                                 cudaStream_t stream) {
+                                 uint32_t* ties, cudaStream_t stream) {
   const unsigned chunk_blocks = static_cast<unsigned>(static_cast<int64_t>(N) * kRowParts);
   if (vec) {
     chunk_sum_kernel<true><<<chunk_blocks, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, accept, chunks);
@@ -661,7 +706,7 @@ cudaError_t launch_residual_pick(const float* p, const float* q, int N, int k, i
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   pick_kernel<<<N, kPickThreads, 0, stream>>>(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks,
-                                              out_tokens);
+                                              out_tokens, ties);
   return cudaGetLastError();
 }
 
@@ -683,7 +728,8 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
 cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                int V, uint64_t seed, uint32_t offset, void* ws,
                                int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
-                               uint32_t u_stream, int u_pos, int64_t row_stride, int64_t token_stride) {
+                               uint32_t u_stream, int u_pos, int64_t row_stride, int64_t token_stride,
+                               uint32_t* ties) {
   if (N == 0) return cudaSuccess;
   const SpecWorkspaceLayout L = spec_workspace_layout(N, k);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -703,11 +749,11 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
     if (vec0) {
       bonus_sample_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, V, stride, seed, offset, u_stream, pos,
                                                                      bonus, arrivals, out_tokens, token_stride,
-                                                                     n_accepted);
+                                                                     n_accepted, ties);
     } else {
       bonus_sample_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, V, stride, seed, offset, u_stream, pos,
                                                                       bonus, arrivals, out_tokens, token_stride,
-                                                                      n_accepted);
+                                                                      n_accepted, ties);
     }
     return cudaGetLastError();
   }
@@ -720,17 +766,21 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   accept_kernel<<<(N + 7) / 8, 256, 0, stream>>>(p, q, drafts, N, k, V, seed, offset, stats, accept,
-                                                  out_tokens, n_accepted, err);
+                                                  out_tokens, n_accepted, err, ties);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, stream);
+  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, ties,
+                              stream);
 }
 
 cudaError_t launch_spec_sample_sequential(const float* p, const float* q, const int32_t* drafts, int N, int k,
                                           int V, uint64_t seed, uint32_t offset, void* ws,
-                                          int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream) {
+                                          int32_t* out_tokens, int32_t* n_accepted, cudaStream_t stream,
+                                          uint32_t* ties) {
   if (N == 0) return cudaSuccess;
-  if (k == 0) return launch_spec_sample(p, q, drafts, N, k, V, seed, offset, ws, out_tokens, n_accepted, stream);
+  if (k == 0)
+    return launch_spec_sample(p, q, drafts, N, k, V, seed, offset, ws, out_tokens, n_accepted, stream, 1, -1, 0, 1,
+                              ties);
   const SpecWorkspaceLayout L = spec_workspace_layout(N, k);
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* err = reinterpret_cast<int*>(w + L.err_off);
@@ -749,16 +799,17 @@ cudaError_t launch_spec_sample_sequential(const float* p, const float* q, const 
     if (vec) {
       seq_step_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, q, drafts, N, k, V, i, seed, offset, stats,
                                                                  bonus, qchunks, accept, arrivals, out_tokens,
-                                                                 n_accepted, err);
+                                                                 n_accepted, err, ties);
     } else {
       seq_step_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, q, drafts, N, k, V, i, seed, offset, stats,
                                                                   bonus, qchunks, accept, arrivals, out_tokens,
-                                                                  n_accepted, err);
+                                                                  n_accepted, err, ties);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, stream);
+  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, ties,
+                              stream);
 }
 
 }  // namespace s3r

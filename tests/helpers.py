@@ -77,3 +77,51 @@ def budget_b_max(num_pages, budget, n_sink=1, n_recent=4):
     P = int(num_pages)
     mand = min(n_sink, P) + (P - max(max(P - n_recent, 0), min(n_sink, P)))
     return max(min(P, max(math.ceil(budget * P - 1e-9), mand)), 1)
+
+
+# Selection ties: the GPU selects from its fp32 page mass, the oracle from its
+# own fp64 mass.  A page where the two choices differ must lie within
+# SELECT_TIE * (rows per KV head) of the cutoff in the oracle's mass (each of
+# the G*T rows contributes mass 1, so the window scales with the row count).
+SELECT_TIE = 1e-6
+
+
+def selection_ties_vs_oracle_mass(sel_gpu, cnt_gpu, mass_ref, sel_lens, budget, rows, n_sink=1, n_recent=4):
+    """Checks a GPU selection against the oracle's selection from the oracle's
+    own mass, and returns the number of tie swaps (pairs of pages, one chosen
+    by each side only, both within the window of the cutoff).
+
+    sel_gpu [S][H][b_max], cnt_gpu [S][H] (GPU, from the GPU's mass);
+    mass_ref [S][H][>= pages] (oracle fp64); sel_lens [S]; rows = G * T."""
+    import oracle
+    sel_gpu, cnt_gpu = np.asarray(sel_gpu), np.asarray(cnt_gpu)
+    mass_ref = np.asarray(mass_ref, dtype=np.float64)
+    S, H = cnt_gpu.shape
+    ref_sel, ref_cnt = oracle.select_draft_pages(mass_ref, sel_lens, budget, n_sink, n_recent,
+                                                 b_max=sel_gpu.shape[-1])
+    assert np.array_equal(cnt_gpu, ref_cnt), "page budgets differ"
+    tol = SELECT_TIE * rows
+    swaps = 0
+    for s in range(S):
+        P = ceil_div(int(sel_lens[s]), 16)
+        B, mandatory = oracle.selection_budget(P, budget, n_sink, n_recent)
+        for h in range(H):
+            c = int(cnt_gpu[s, h])
+            g = sel_gpu[s, h, :c]
+            assert np.all(np.diff(g) > 0), f"({s},{h}): GPU selection not ascending"
+            assert np.all(sel_gpu[s, h, c:] == -1)
+            gs, rs = set(g.tolist()), set(ref_sel[s, h, :c].tolist())
+            if gs == rs:
+                continue
+            assert mandatory <= gs, f"({s},{h}): a mandatory page is missing"
+            rest = sorted(rs - mandatory, key=lambda pg: (-mass_ref[s, h, pg], pg))
+            cutoff = mass_ref[s, h, rest[-1]]
+            only_g, only_r = gs - rs, rs - gs
+            for pg in only_g:
+                assert mass_ref[s, h, pg] >= cutoff - tol, \
+                    f"({s},{h}) page {pg}: mass {mass_ref[s, h, pg]:.9g} vs cutoff {cutoff:.9g}"
+            for pg in only_r:
+                assert mass_ref[s, h, pg] <= cutoff + tol, \
+                    f"({s},{h}) page {pg}: mass {mass_ref[s, h, pg]:.9g} vs cutoff {cutoff:.9g}"
+            swaps += len(only_g)
+    return swaps

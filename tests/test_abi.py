@@ -76,16 +76,16 @@ def test_argument_validation_on_host(lib):
     assert lib.s3r_select_draft_pages(None, None, 1, 8, 8, ctypes.c_double(1.5), 1, 4, None, None, 8,
                                       None, 0, None) == 1
     # spec sample: k above the limit, empty vocabulary, offset beyond 32 bits
-    assert lib.s3r_spec_sample(None, None, None, 1, 65, 10, 0, 0, None, None, None, 0, None) == 2
-    assert lib.s3r_spec_sample(None, None, None, 1, 4, 0, 0, 0, None, None, None, 0, None) == 1
-    assert lib.s3r_spec_sample(None, None, None, 1, 4, 10, 0, 1 << 32, None, None, None, 0, None) == 1
+    assert lib.s3r_spec_sample(None, None, None, 1, 65, 10, 0, 0, None, None, None, None, 0, None) == 2
+    assert lib.s3r_spec_sample(None, None, None, 1, 4, 0, 0, 0, None, None, None, None, 0, None) == 1
+    assert lib.s3r_spec_sample(None, None, None, 1, 4, 10, 0, 1 << 32, None, None, None, None, 0, None) == 1
 
 
 def test_new_entry_points_validate_on_host(lib):
     kv = _kv()
     # the sequential sampler shares the parallel sampler's checks
-    assert lib.s3r_spec_sample_sequential(None, None, None, 1, 65, 10, 0, 0, None, None, None, 0, None) == 2
-    assert lib.s3r_spec_sample_sequential(None, None, None, -1, 4, 10, 0, 0, None, None, None, 0, None) == 1
+    assert lib.s3r_spec_sample_sequential(None, None, None, 1, 65, 10, 0, 0, None, None, None, None, 0, None) == 2
+    assert lib.s3r_spec_sample_sequential(None, None, None, -1, 4, 10, 0, 0, None, None, None, None, 0, None) == 1
     # draft sampling: rows closer than the vocabulary, token stride 0, missing workspace
     assert lib.s3r_sample_draft_tokens(None, 4, 100, 99, 0, 0, 0, None, 1, None, 0, None) == 1
     assert lib.s3r_sample_draft_tokens(None, 4, 100, 100, 0, 0, 0, None, 0, None, 0, None) == 1
@@ -133,3 +133,13 @@ def test_fused_append_calls_validate_rows_on_host(lib):
     assert verify(3, None) == 1
     assert verify(3, rows(2)) == 1               # the block's T rows
     assert verify(3, rows(3, k=0x90004)) == 1
+
+
+def test_no_alloc_checks_arguments_before_touching_its_scratch(lib):
+    # Each bad argument is reported as S3R_ERR_INVALID_ARG.  Without a GPU the
+    # scratch lookup would fail with S3R_ERR_CUDA, so these statuses also show
+    # that the checks run before the shared scratch (and any clear of it).
+    assert lib.s3r_spec_sample_noalloc(None, None, None, 4, 2, 0, 0, 0, None, None, None, None) == 1
+    assert lib.s3r_spec_sample_noalloc(None, None, None, 4, 2, 10, 0, 1 << 32, None, None, None, None) == 1
+    assert lib.s3r_spec_sample_noalloc(None, None, None, 4, 2, 10, 0, 0, None, None, None, None) == 1
+    assert lib.s3r_spec_sample_noalloc(None, None, None, -1, 2, 10, 0, 0, None, None, None, None) == 1

@@ -4,7 +4,10 @@ Tolerances (the bar for attention outputs, fp32 on the GPU side): max-abs
 <= 1e-2 and mean-relative (mean |gpu - ref| / mean |ref|) <= 2e-3 over all
 output elements.  Page mass:
 |gpu - ref| <= 1e-4 * mass + 1e-6 * rows, and every (sequence, KV head) row of
-mass sums to its row count."""
+mass sums to its row count.  Selection, end to end: the GPU's pages, chosen
+from the GPU's mass, equal the oracle's pages chosen from the oracle's own
+fp64 mass, except swaps of pages within 1e-6 * rows of the cutoff, which are
+counted and printed."""
 
 import math
 
@@ -16,7 +19,8 @@ import oracle
 import speculative_decode_attention_paged_b300 as s3r
 from workloads import (ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_8B_128SEQ, ATTN_TINY, bf16_to_bits, make_paged_kv,
                        make_queries)
-from helpers import (assert_attn_close, attn_workspace, compact_pool, host, kv_desc, run_verify_select)
+from helpers import (assert_attn_close, attn_workspace, budget_b_max, compact_pool, host, kv_desc, run_verify_select,
+                     selection_ties_vs_oracle_mass)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -86,6 +90,16 @@ def test_verify_ragged_with_mass(q_heads, kv_heads, T):
     _check_mass(mass, mref, G * T)
     sums = host(mass).astype(np.float64).sum(axis=-1)
     np.testing.assert_allclose(sums, G * T, rtol=1e-4)
+    # verify -> mass -> select on the GPU against the oracle's selection from its own mass
+    sel_lens = (kv.hist_lens + T).to(torch.int32)
+    for budget in (0.1, 0.3):
+        b_max = budget_b_max(mass.shape[-1], budget)
+        sel = torch.empty((len(lens), kv_heads, b_max), dtype=torch.int32, device=DEV)
+        cnt = torch.empty((len(lens), kv_heads), dtype=torch.int32, device=DEV)
+        s3r.s3r_select_draft_pages(mass, sel_lens, budget, sel, cnt, ws)
+        ws.check()
+        swaps = selection_ties_vs_oracle_mass(host(sel), host(cnt), mref, host(sel_lens), budget, G * T)
+        assert swaps <= 2, swaps
 
 
 def test_verify_without_mass_matches_with_mass():
@@ -234,6 +248,11 @@ def _full_round_check(cfg, budget, n_check, seed_q=500):
                                                  b_max=sel.shape[-1])
     assert np.array_equal(host(cnt[seqs]), cnt_ref)
     assert np.array_equal(host(sel[seqs]), sel_ref)
+    # and, end to end, the oracle's selection from its own fp64 mass, up to counted ties
+    swaps = selection_ties_vs_oracle_mass(host(sel[seqs]), host(cnt[seqs]), mref, host(sel_lens)[seqs], budget,
+                                          G * T)
+    print(f"{cfg.name} budget {budget}: {swaps} selection tie swaps over {n_check * cfg.kv_heads} pairs")
+    assert swaps <= max(2, n_check * cfg.kv_heads // 100)
     for j in range(T):
         ref_d = oracle.sparse_draft_attn(bf16_to_bits(qd[j][seqs]), kp, vp, bt, host(kv2_hist)[seqs], j,
                                          host(sel[seqs]), host(cnt[seqs]), 1.0)

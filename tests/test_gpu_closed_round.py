@@ -10,8 +10,9 @@ stage against the oracle on the inputs each GPU stage consumed:
 The second round starts from the first round's L' and selection.  Pools are compared bit for
 bit, attention with the attention tolerances, page mass with the mass
 tolerance, tokens and accepted counts exactly up to the sampler's tie rules,
-lengths and selections exactly (the selection oracle reads the GPU's fp32
-mass)."""
+lengths exactly, and selections exactly when the selection oracle reads the
+GPU's fp32 mass and up to counted cutoff ties when it reads its own fp64
+mass."""
 
 import math
 
@@ -22,7 +23,7 @@ from scipy import special
 
 import oracle
 import speculative_decode_attention_paged_b300 as s3r
-from helpers import assert_attn_close, budget_b_max, host, kv_desc
+from helpers import assert_attn_close, budget_b_max, host, kv_desc, selection_ties_vs_oracle_mass
 from test_gpu_attention import _check_mass
 from test_gpu_spec_sample import CDF_TIE, compare
 from workloads import bf16_to_bits, make_paged_kv, make_queries, make_spec_inputs
@@ -111,6 +112,7 @@ def test_two_closed_rounds_two_layers():
         sws.check()
         # ---- stage by stage against the oracle
         x = host(drafts)
+        ref_masses = []
         for j in range(K):
             _check_draft_tokens(host(q_logits[:, j]), x[:, j], SEED, OFFSET, j)
         for li, kv in enumerate(kvs):
@@ -129,6 +131,7 @@ def test_two_closed_rounds_two_layers():
             ref_o, ref_m = oracle.verify_attn(bf16_to_bits(qv[li]), kp, vp, bt, Lh, 1.0, mass_pages=max_pages)
             assert_attn_close(out_v[li], ref_o, f"round {rnd} layer {li} verify")
             _check_mass(mass[li], ref_m, (HQ // HKV) * (K + 1))
+            ref_masses.append(ref_m)
         compare(host(p_logits), host(q_logits), x, SEED, OFFSET, host(out_t), host(nacc))
         assert np.array_equal(host(L_new), oracle.commit_lengths(Lh, host(nacc)))
         for li in range(LAYERS):
@@ -136,6 +139,9 @@ def test_two_closed_rounds_two_layers():
                                                            b_max=b_max)
             assert np.array_equal(host(new_sel[li][1]), ref_cnt)
             assert np.array_equal(host(new_sel[li][0]), ref_pages)
+            swaps = selection_ties_vs_oracle_mass(host(new_sel[li][0]), host(new_sel[li][1]), ref_masses[li],
+                                                  host(L_new), BUDGET, (HQ // HKV) * (K + 1))
+            assert swaps <= 1, swaps
         assert np.all(host(new_sel[0][1]) == np.array([[budget_b_max(math.ceil(x / 16), BUDGET)] * HKV
                                                         for x in host(L_new)]))
         L, sel = L_new, new_sel

@@ -2,9 +2,9 @@
 
 It computes the same function as the parallel sampler with the ratio tests
 taken one position at a time, so on the same inputs its accepted counts and
-tokens must equal the parallel sampler's bit for bit; against the oracle the
-same tie rules apply (ratio ties within 1e-6, inverse-CDF ties within
-2e-6 * Z).  Its per-sequence arrival counters must be left at zero, so a
+tokens must equal the parallel sampler's bit for bit, and so must its tie
+counts; against the oracle the same tie rules apply (ratio ties within 1e-6,
+inverse-CDF ties within 1e-6 * Z).  Its per-sequence arrival counters must be left at zero, so a
 workspace serves any number of calls."""
 
 import numpy as np
@@ -20,22 +20,26 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(fn, p, q, x, seed, offset=0, ws=None):
+def _run(fn, p, q, x, seed, offset=0, ws=None, ties=None):
     N, k1, V = p.shape
     if ws is None:
         ws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(N, k1 - 1))
     out = torch.full((N, k1), 77, dtype=torch.int32, device=DEV)
     nacc = torch.full((N,), 77, dtype=torch.int32, device=DEV)
-    fn(p, q, x, seed, offset, out, nacc, ws)
+    fn(p, q, x, seed, offset, out, nacc, ws, tie_count=ties)
     return host(out), host(nacc), ws
 
 
 def _both(inp, seed, offset=0):
-    out_p, nacc_p, ws = _run(s3r.s3r_spec_sample, inp.p_logits, inp.q_logits, inp.draft_tokens, seed, offset)
+    ties_p = torch.full((2,), 55, dtype=torch.int32, device=DEV)
+    ties_s = torch.full((2,), 66, dtype=torch.int32, device=DEV)
+    out_p, nacc_p, ws = _run(s3r.s3r_spec_sample, inp.p_logits, inp.q_logits, inp.draft_tokens, seed, offset,
+                             ties=ties_p)
     ws.check()
     out_s, nacc_s, ws = _run(s3r.s3r_spec_sample_sequential, inp.p_logits, inp.q_logits, inp.draft_tokens, seed,
-                             offset)
+                             offset, ties=ties_s)
     ws.check()
+    assert torch.equal(ties_p, ties_s)
     return (out_p, nacc_p), (out_s, nacc_s)
 
 

@@ -16,6 +16,7 @@ import oracle.kv_cache as okv
 import oracle.scheduler as osched
 import oracle.philox as ophil
 import oracle.selection as osel
+import oracle as oracle_pkg
 import oracle.spec_sample  # noqa: F401  (the package re-exports a function of the same name)
 import test_oracle_attention as pins_att
 import test_oracle_draft_sample as pins_draft
@@ -152,3 +153,17 @@ def test_new_requests_ahead_of_paused_ones_is_caught(monkeypatch):
     mutant = _mutant(osched, "simulate", "            if paused:\n", "            if paused and not waiting:\n")
     monkeypatch.setattr(pins_sched, "simulate", mutant)
     _fails(pins_sched.test_invariants_on_random_workloads, osched.POLICY_AIMD, 1)
+
+
+def test_tie_judge_residual_with_wrong_sign_is_caught(monkeypatch):
+    mutant = _mutant(ospec, "residual_row", "r = np.maximum(p - q, 0.0)", "r = np.maximum(q - p, 0.0)")
+    monkeypatch.setattr(ospec, "residual_row", mutant)
+    monkeypatch.setattr(oracle_pkg, "residual_row", mutant)
+    _fails(pins_spec.test_residual_of_disjoint_supports_is_the_target)
+
+
+def test_tie_judge_residual_without_fallback_is_caught(monkeypatch):
+    mutant = _mutant(ospec, "residual_row", "        return p\n", "        return r\n")
+    monkeypatch.setattr(ospec, "residual_row", mutant)
+    monkeypatch.setattr(oracle_pkg, "residual_row", mutant)
+    _fails(pins_spec.test_residual_of_equal_rows_falls_back_to_the_target)

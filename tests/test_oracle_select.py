@@ -75,3 +75,28 @@ def test_invariants_random():
                 left = [pg for pg in rest if pg not in picked]
                 if picked and left:
                     assert min(mass[s, h, picked]) >= max(mass[s, h, left])
+
+
+def test_selection_tie_judge_accepts_only_cutoff_swaps():
+    """The GPU tests judge a selection made from fp32 mass against the oracle's
+    selection from fp64 mass; the judge must accept a swap of the two pages
+    that straddle the cutoff within the window and reject any other swap."""
+    import pytest
+    from helpers import SELECT_TIE, selection_ties_vs_oracle_mass
+    rows = 8
+    P = 40          # 640 tokens; budget 0.25 -> B = 10: pages 0 and 36..39, then 1..5 by mass
+    mass = np.linspace(1.0, 0.2, P)[None, None, :].copy()
+    mass[0, 0, 20] = mass[0, 0, 5] - 0.5 * SELECT_TIE * rows     # a near-tie with the cutoff page 5
+    sel_lens = np.array([P * 16])
+    ref_sel, ref_cnt = select_draft_pages(mass, sel_lens, 0.25, 1, 4, b_max=12)
+    assert selection_ties_vs_oracle_mass(ref_sel, ref_cnt, mass, sel_lens, 0.25, rows) == 0
+    chosen = [int(x) for x in ref_sel[0, 0, : ref_cnt[0, 0]]]
+    assert 5 in chosen and 20 not in chosen
+    swapped = np.full_like(ref_sel, -1)
+    good = sorted(set(chosen) - {5} | {20})
+    swapped[0, 0, : len(good)] = good
+    assert selection_ties_vs_oracle_mass(swapped, ref_cnt, mass, sel_lens, 0.25, rows) == 1
+    bad = sorted(set(chosen) - {5} | {30})      # page 30 lies far below the cutoff
+    swapped[0, 0, : len(bad)] = bad
+    with pytest.raises(AssertionError):
+        selection_ties_vs_oracle_mass(swapped, ref_cnt, mass, sel_lens, 0.25, rows)

@@ -96,3 +96,39 @@ def test_disjoint_support_always_rejects_and_emits_from_target():
     counts = np.bincount(out[:, 0], minlength=V)
     assert counts[4:].sum() == 0
     assert stats.chisquare(counts[:4]).pvalue > 1e-3
+
+
+# ---------------------------------------------------------------- residual_row
+# residual_row is the row the oracle resamples from after a rejection, and the
+# GPU parity tests use it to judge inverse-CDF ties.  Its pins: the residual of
+# disjoint supports is p itself; p = q falls back to p; the closed form
+# sum_v max(0, p - q) = 1 - sum_v min(p, q) (the rejection probability); and
+# the residual's support is exactly {v : p(v) > q(v)}.
+
+def test_residual_of_disjoint_supports_is_the_target():
+    from oracle import residual_row
+    p_logits = np.array([0.0, 1.0, -1e4, -1e4, 0.5])
+    q_logits = np.array([-1e4, -1e4, 0.0, 2.0, -1e4])
+    p = special.softmax(p_logits)
+    r = residual_row(p_logits, q_logits)
+    np.testing.assert_allclose(r, p, rtol=0, atol=1e-15)
+
+
+def test_residual_of_equal_rows_falls_back_to_the_target():
+    from oracle import residual_row
+    x = np.random.default_rng(21).normal(0, 2.0, size=37)
+    np.testing.assert_allclose(residual_row(x, x), special.softmax(x), rtol=0, atol=1e-15)
+
+
+def test_residual_total_is_the_rejection_probability():
+    from oracle import residual_row
+    rng = np.random.default_rng(22)
+    for V in (2, 9, 1000):
+        p_logits = rng.normal(0, 3.0, size=V)
+        q_logits = p_logits + rng.normal(0, 1.0, size=V)
+        p, q = special.softmax(p_logits), special.softmax(q_logits)
+        r = residual_row(p_logits, q_logits)
+        assert abs(r.sum() - (1.0 - np.minimum(p, q).sum())) < 1e-12
+        assert np.all(r >= 0.0)
+        # support: positive exactly where the target outweighs the draft
+        assert np.array_equal(r > 0.0, p > q)
