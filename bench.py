@@ -49,8 +49,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from workloads import (ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_1P7B_28LAYER, ATTN_QWEN3_8B_128SEQ,  # noqa: E402
-                       SAMPLER_ROLLOUT_2048SEQ, SAMPLER_ROUND_256SEQ, make_paged_kv, make_queries,
-                       make_rollout_requests, make_spec_inputs)
+                       ATTN_TINY, ROLLOUT_ACCEPTANCE_MATCHED_SIGMAS, SAMPLER_ROLLOUT_2048SEQ, SAMPLER_ROUND_256SEQ,
+                       SAMPLER_TINY, make_paged_kv, make_queries, make_rollout_requests, make_spec_inputs)
 
 METRIC = "KV GB/s (% of 8 TB/s) and draft+verify attention tokens/s at 1 B300"
 UNIT = "GB/s"
@@ -306,75 +306,137 @@ def allreduce_max(x, world):
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
 
-_ORACLE_INPUTS = {}
-
-
-def oracle_sample(seconds, seed=0):
-    """Run the fp64 oracle over whole sequences of a host-sized slice of the
-    same workload until `seconds` of CPU work are spent; returns (bytes, time,
-    description).  The slice is regenerated on the CPU with the same recipe
-    (same shapes and distributions, fewer sequences)."""
-    import oracle
+def _oracle_inputs(seed, n_seqs):
+    """Host inputs of `n_seqs` sequences of the 256-sequence round, regenerated
+    on the CPU with the same recipe (shapes, distributions) and their own seed."""
     from workloads import bf16_to_bits
-
     c = ATTN_QWEN3_1P7B_256SEQ
     sc = SAMPLER_ROUND_256SEQ
-    n_seqs = 8
-    if seed not in _ORACLE_INPUTS:
-        _ORACLE_INPUTS.clear()
-        kv = make_paged_kv(n_seqs, c.q_heads, c.kv_heads, 2 * c.k, seed=c.seed + 100 + seed, device="cpu",
-                           hist_min=c.hist_min, hist_max=c.hist_max)
-        spec = make_spec_inputs(n_seqs, sc.k, sc.vocab, sc.p_sigma, sc.q_sigmas[0], sc.seed + 100 + seed)
-        _ORACLE_INPUTS[seed] = (
-            bf16_to_bits(kv.k_pool), bf16_to_bits(kv.v_pool), kv.block_table.numpy(),
+    kv = make_paged_kv(n_seqs, c.q_heads, c.kv_heads, 2 * c.k, seed=c.seed + 100 + seed, device="cpu",
+                       hist_min=c.hist_min, hist_max=c.hist_max)
+    spec = make_spec_inputs(n_seqs, sc.k, sc.vocab, sc.p_sigma, sc.q_sigmas[0], sc.seed + 100 + seed)
+    return (bf16_to_bits(kv.k_pool), bf16_to_bits(kv.v_pool), kv.block_table.numpy(),
             kv.hist_lens.numpy().astype(np.int64), bf16_to_bits(make_queries(kv, 1000, rows=c.k)),
             bf16_to_bits(make_queries(kv, 1100)), spec.p_logits.numpy(), spec.q_logits.numpy(),
             spec.draft_tokens.numpy())
-    kp, vp, bt, L, qv, qd, p_l, q_l, x_l = _ORACLE_INPUTS[seed]
-    k = c.k
-    Hkv, Hq = c.kv_heads, c.q_heads
-    done_bytes = 0.0
+
+
+def _oracle_pass(inputs, s):
+    """The fp64 oracle over one whole sequence s of `inputs`: k dense decode
+    steps, verify with page mass, selection, k sparse drafts and exact
+    speculative sampling; returns the algorithmic bytes of that work."""
+    import oracle
+    c = ATTN_QWEN3_1P7B_256SEQ
+    sc = SAMPLER_ROUND_256SEQ
+    kp, vp, bt, L, qv, qd, p_l, q_l, x_l = inputs
+    n_seqs = len(L)
+    k, Hkv, Hq = c.k, c.kv_heads, c.q_heads
+    one = [s]
+    done = 0.0
+    for j in range(k):
+        oracle.dense_decode_attn(qd, kp, vp, bt, L + j + 1, 1.0, seqs=one)
+        done += (L[s] + j + 1) * Hkv * KV_TOKEN_BYTES_PER_HEAD + Hq * 128 * 6
+    _, mass = oracle.verify_attn(qv, kp, vp, bt, L, 1.0, seqs=one, mass_pages=bt.shape[1])
+    done += (L[s] + k) * Hkv * KV_TOKEN_BYTES_PER_HEAD + k * Hq * 128 * 6 + Hkv * bt.shape[1] * 4
+    sel, cnt = oracle.select_draft_pages(mass, L[one] + k, c.budgets[0], 1, 4)
+    done += Hkv * (bt.shape[1] + sel.shape[-1]) * 4
+    sel_full = np.full((n_seqs, Hkv, sel.shape[-1]), -1, dtype=np.int64)
+    cnt_full = np.zeros((n_seqs, Hkv), dtype=np.int64)
+    sel_full[s], cnt_full[s] = sel[0], cnt[0]
+    for j in range(k):
+        oracle.sparse_draft_attn(qd, kp, vp, bt, L + k, j, sel_full, cnt_full, 1.0, seqs=one)
+        vis = 0
+        for h in range(Hkv):
+            pg = sel[0, h, : cnt[0, h]]
+            vis += int(np.minimum(pg * 16 + 16, L[s] + k).sum() - np.minimum(pg * 16, L[s] + k).sum()) + j + 1
+        done += vis * KV_TOKEN_BYTES_PER_HEAD + Hq * 128 * 6
+    oracle.spec_sample(p_l[one], q_l[one], x_l[one], sc.philox_seed, 0, seq_ids=one)
+    done += (2 * sc.k + 1) * sc.vocab * 4
+    return done
+
+
+def _oracle_loop(inputs, seconds):
+    """Whole-sequence oracle passes over `inputs` until `seconds` of CPU time
+    are spent (at least one pass); returns (bytes, seconds, passes)."""
+    n = len(inputs[3])
+    done, passes = 0.0, 0
     t0 = time.perf_counter()
-    seqs_done = 0
-    for it in range(1 << 20):
-        s = it % n_seqs
-        one = [s]
-        for j in range(k):
-            oracle.dense_decode_attn(qd, kp, vp, bt, L + j + 1, 1.0, seqs=one)
-            done_bytes += (L[s] + j + 1) * Hkv * KV_TOKEN_BYTES_PER_HEAD + Hq * 128 * 6
-        _, mass = oracle.verify_attn(qv, kp, vp, bt, L, 1.0, seqs=one, mass_pages=bt.shape[1])
-        done_bytes += (L[s] + k) * Hkv * KV_TOKEN_BYTES_PER_HEAD + k * Hq * 128 * 6 + Hkv * bt.shape[1] * 4
-        sel, cnt = oracle.select_draft_pages(mass, L[one] + k, c.budgets[0], 1, 4)
-        done_bytes += Hkv * (bt.shape[1] + sel.shape[-1]) * 4
-        sel_full = np.full((n_seqs, Hkv, sel.shape[-1]), -1, dtype=np.int64)
-        cnt_full = np.zeros((n_seqs, Hkv), dtype=np.int64)
-        sel_full[s], cnt_full[s] = sel[0], cnt[0]
-        for j in range(k):
-            oracle.sparse_draft_attn(qd, kp, vp, bt, L + k, j, sel_full, cnt_full, 1.0, seqs=one)
-            vis = 0
-            for h in range(Hkv):
-                pg = sel[0, h, : cnt[0, h]]
-                vis += int(np.minimum(pg * 16 + 16, L[s] + k).sum() - np.minimum(pg * 16, L[s] + k).sum()) + j + 1
-            done_bytes += vis * KV_TOKEN_BYTES_PER_HEAD + Hq * 128 * 6
-        oracle.spec_sample(p_l[one], q_l[one], x_l[one], sc.philox_seed, 0, seq_ids=one)
-        done_bytes += (2 * sc.k + 1) * sc.vocab * 4
-        seqs_done += 1
-        if time.perf_counter() - t0 >= seconds or (seconds <= 0 and seqs_done == n_seqs):
+    while True:
+        done += _oracle_pass(inputs, passes % n)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
             break
-    dt = time.perf_counter() - t0
-    desc = (f"{seqs_done} sequence passes over {min(seqs_done, n_seqs)} distinct sequences of the 256-sequence step (same recipe, histories U{{4096..16384}}): "
-            f"{k} dense decode steps, verify+mass, select, {k} sparse drafts, spec sample over V={sc.vocab}; "
-            f"fp64 NumPy oracle")
-    return done_bytes, dt, desc
+    return done, time.perf_counter() - t0, passes
 
 
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        info = threadpool_info()
-        return max([d.get("num_threads", 1) for d in info] + [1])
-    except Exception:
-        return 1
+def _oracle_worker(wid, n_seqs, cmd_q, res_q, barrier):
+    """One oracle process of OracleFarm: builds its own sequences, then runs a
+    timed loop for each command until it receives None."""
+    inputs = _oracle_inputs(1000 + wid, n_seqs)
+    res_q.put(("ready", wid))
+    while True:
+        seconds = cmd_q.get()
+        if seconds is None:
+            return
+        barrier.wait()
+        res_q.put(_oracle_loop(inputs, seconds))
+
+
+_SINGLE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+class OracleFarm:
+    """The fp64 oracle on the host's cores: one single-threaded process per
+    core (started with spawn, so no CUDA state is inherited), each over its
+    own sequences of the same recipe.  run(seconds) times all of them
+    together and returns (bytes, wall seconds, passes): the oracle's whole-job
+    throughput on `workers` cores."""
+
+    def __init__(self, workers=None, seqs_per_worker=2):
+        import multiprocessing as mp
+        self.cpu_count = os.cpu_count() or 1
+        # one per core, at most 128 (about 0.3 GB of host memory each)
+        self.workers = max(1, int(workers or min(self.cpu_count, 128)))
+        ctx = mp.get_context("spawn")
+        self.cmd = [ctx.Queue() for _ in range(self.workers)]
+        self.res = ctx.Queue()
+        self.barrier = ctx.Barrier(self.workers)
+        saved = {k: os.environ.get(k) for k in _SINGLE_THREAD_ENV}
+        for k in _SINGLE_THREAD_ENV:
+            os.environ[k] = "1"
+        try:
+            self.procs = [ctx.Process(target=_oracle_worker, args=(i, seqs_per_worker, self.cmd[i], self.res,
+                                                                   self.barrier), daemon=True)
+                          for i in range(self.workers)]
+            for pr in self.procs:
+                pr.start()
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for _ in range(self.workers):
+            self.res.get(timeout=600)
+        self.seqs = self.workers * seqs_per_worker
+
+    def run(self, seconds):
+        for q in self.cmd:
+            q.put(float(seconds))
+        out = [self.res.get(timeout=600 + 10 * seconds) for _ in range(self.workers)]
+        return sum(o[0] for o in out), max(o[1] for o in out), sum(o[2] for o in out)
+
+    def close(self):
+        for q in self.cmd:
+            q.put(None)
+        for pr in self.procs:
+            pr.join(timeout=30)
+
+    def describe(self, passes, seconds):
+        return (f"{passes} whole-sequence passes in {seconds:.1f} s by {self.workers} single-threaded oracle "
+                f"processes ({self.cpu_count} host cores), {self.seqs} distinct sequences of the 256-sequence "
+                f"round's recipe (histories U{{4096..16384}}): 4 dense decode steps, verify+mass, select, "
+                f"4 sparse drafts, spec sample over V=151936; fp64 NumPy oracle")
 
 
 # ---------------------------------------------------------------- arms
@@ -382,15 +444,21 @@ def blas_threads():
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    per_step = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
-    for _ in range(args.warmup):
-        oracle_sample(per_step / 4)
-    total_b, total_t, desc = 0.0, 0.0, ""
-    for i in range(args.steps):
-        b, t, desc = oracle_sample(per_step)
-        total_b += b
-        total_t += t
+    farm = OracleFarm(args.cpu_workers)
+    try:
+        per_step = max(1.0, 60.0 / max(args.steps + args.warmup, 1))
+        for _ in range(args.warmup):
+            farm.run(per_step / 4)
+        total_b, total_t, passes = 0.0, 0.0, 0
+        for _ in range(args.steps):
+            b, t, n = farm.run(per_step)
+            total_b += b
+            total_t += t
+            passes += n
+    finally:
+        farm.close()
     value = total_b / total_t / 1e9
+    desc = farm.describe(passes, total_t)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
@@ -398,17 +466,129 @@ def run_reference(args, world, rank):
         "config": {"workload": "qwen3-1.7b-geom 1 layer, 256 seqs x U{4096..16384}, 16/8 heads, d=128, k=4, "
                                "budget 0.05, vocab 151936 (bounded sample per step)",
                    "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": farm.workers, "cpu_count": farm.cpu_count,
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
+def selection_tie_sample(w, n=8):
+    """The round's selection (from the GPU's fp32 mass) against the oracle's
+    selection from its own fp64 verify mass, on n sequences spread over the
+    batch: pages chosen by one side only are cutoff ties when the oracle's
+    mass of the page lies within 1e-6 * (G * T) of the cutoff, mismatches
+    otherwise."""
+    import oracle
+    from workloads import bf16_to_bits
+    seqs = sorted({int(x) for x in np.linspace(0, w.S - 1, n)})
+    idx = torch.as_tensor(seqs, device=w.kv.block_table.device, dtype=torch.long)
+    bt = w.kv.block_table[idx].long()
+    uniq, inv = torch.unique(bt[bt >= 0], return_inverse=True)
+    bt_c = torch.full_like(bt, -1)
+    bt_c[bt >= 0] = inv
+    kp, vp = bf16_to_bits(w.kv.k_pool[uniq]), bf16_to_bits(w.kv.v_pool[uniq])
+    L = w.kv.hist_lens.cpu().numpy().astype(np.int64)[seqs]
+    _, mref = oracle.verify_attn(bf16_to_bits(w.q_verify[idx]), kp, vp, bt_c.cpu().numpy(), L, 1.0,
+                                 mass_pages=w.mass_stride)
+    sel_lens = w.sel_lens.cpu().numpy()[seqs]
+    ref_sel, ref_cnt = oracle.select_draft_pages(mref, sel_lens, w.budget, 1, 4, b_max=w.b_max)
+    sel, cnt = w.sel[idx].cpu().numpy(), w.cnt[idx].cpu().numpy()
+    tol = 1e-6 * (w.Hq // w.Hkv) * w.k
+    ties = mismatched = 0
+    for i in range(len(seqs)):
+        P = ceil_div(int(sel_lens[i]), 16)
+        mand = set(range(min(1, P))) | set(range(max(P - 4, 0), P))
+        for h in range(w.Hkv):
+            g = set(sel[i, h, : cnt[i, h]].tolist())
+            r = set(ref_sel[i, h, : ref_cnt[i, h]].tolist())
+            if g == r:
+                continue
+            rest = sorted(r - mand, key=lambda pg: (-mref[i, h, pg], pg))
+            cut = mref[i, h, rest[-1]] if rest else 0.0
+            for pg in g - r:
+                ties, mismatched = (ties + 1, mismatched) if mref[i, h, pg] >= cut - tol else (ties, mismatched + 1)
+            for pg in r - g:
+                if mref[i, h, pg] > cut + tol:
+                    mismatched += 1
+    return {"pairs": len(seqs) * w.Hkv, "tie_swaps": ties, "mismatched_pages": mismatched,
+            "window": "1e-6 x G x T of the oracle's fp64 mass"}
+
+
+def run_tiny(args):
+    """The 4-sequence x 2048-token case (one layer, 16 q / 8 KV heads, k = 4,
+    budget 0.10; sampler 4 x k = 4 x V = 4096): latency per call of every
+    step, through the same binding calls as the round (L2-resident: a latency
+    case, not a bandwidth one)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = Workload(dev, attn_cfg=ATTN_TINY, sampler_cfg=SAMPLER_TINY)
+    r = Runner(w)
+    for _ in range(max(3, args.warmup)):
+        r.step()
+    torch.cuda.synchronize()
+    n = 50
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(r.n_events())] for _ in range(n)]
+    for i in range(n):
+        r.step(evs[i])
+    torch.cuda.synchronize()
+    r.ws.check()
+    r.sws.check()
+    k = w.k
+    d = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(r.n_events() - 1)] for e in evs]) * 1e3
+    return {"workload": "4 seqs x 2048 tokens, 16 q / 8 kv heads, k=4, budget 0.10; sampler 4 x k=4 x V=4096",
+            "dense_decode_us": float(d[:, 0:k].mean()), "verify_mass_us": float(d[:, k].mean()),
+            "select_us": float(d[:, k + 1].mean()), "sparse_draft_us": float(d[:, k + 2: 2 * k + 2].mean()),
+            "spec_sample_us": float(d[:, 2 * k + 2].mean()), "calls_timed": n}
+
+
+def run_extras(args):
+    """Compact results of the other workloads for the default bench line (each
+    leg at up to 10 timed steps; a leg that fails reports its error instead)."""
+    sub = argparse.Namespace(**vars(args))
+    sub.steps, sub.warmup, sub.seqs, sub.layers, sub.all_16k = min(args.steps, 10), 3, None, None, False
+    out = {}
+
+    def sweep_c(r):
+        return {"dense_gbs": r["dense"]["gbs"], "verify_T8_G4_ms": r["verify_T8_G4"]["ms"],
+                "verify_T8_G4_gbs": r["verify_T8_G4"]["gbs"],
+                "budgets": {b: {"draft_kv_gb_per_step": v["draft_kv_gb_per_step"], "draft_gbs": v["draft_gbs"],
+                                "draft_ms_per_step": v["draft_ms_per_step"],
+                                "draft_verify_tokens_per_s": v["draft_verify_tokens_per_s"]}
+                            for b, v in r["budgets"].items()}}
+
+    def sampler_c(r):
+        return {sg: {"gbs": v["gbs"], "ms": v["ms"], "recipe": v["recipe"], "mean_accepted": v["mean_accepted"],
+                     "per_position_acceptance": float(np.mean(v["per_position_acceptance"])),
+                     "sampled_tokens_per_s": v["sampled_tokens_per_s"], "ratio_ties": v["ratio_ties"],
+                     "cdf_ties": v["cdf_ties"], "sequential_ms": v["sequential"]["ms"]}
+                for sg, v in r["sigma"].items()}
+
+    def layers_c(r):
+        return {k_: r[k_] for k_ in ("value", "round_ms", "dense_4_steps_ms", "round_vs_4_dense_time",
+                                     "emitted_tokens_speedup", "s3r_emitted_tokens_per_s",
+                                     "dense_emitted_tokens_per_s", "mean_accepted", "round_gb")}
+
+    legs = (("tiny_4seq_2048_latency", run_tiny, lambda r: {k_: v for k_, v in r.items() if k_ != "workload"}),
+            ("qwen3_8b_128seq_sweep", run_sweep, sweep_c),
+            ("sampler_2048seq_k8", run_sampler, sampler_c),
+            ("layers_28_closed_round", run_layers, layers_c))
+    for name, fn, compact in legs:
+        try:
+            out[name] = compact(fn(sub))
+        except Exception as e:  # one leg's failure must not cost the contract line
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_s3r(args, world, rank, local):
     import speculative_decode_attention_paged_b300 as s3r
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    # the oracle's processes start before the first GPU call (spawned: no CUDA state is inherited)
+    farm = OracleFarm(args.cpu_workers) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     s3r.load_library()
     dev = torch.device("cuda", torch.cuda.current_device())
     w = Workload(dev, num_seqs=args.seqs)
@@ -493,6 +673,18 @@ def run_s3r(args, world, rank, local):
     # ---- end to end: host (pinned) inputs -> device -> C-ABI calls -> host results
     e2e = run_e2e(w, r, max(4, min(K, 10)), world)
 
+    # ---- tie accounting of the round (untimed): the sampler's own counters and
+    # the selection against the oracle's fp64 mass on sampled sequences
+    ties = torch.zeros((2,), dtype=torch.int32, device=dev)
+    s3r.s3r_spec_sample(w.spec.p_logits, w.spec.q_logits, w.spec.draft_tokens, w.scfg.philox_seed, 0,
+                        w.out_tokens, w.n_acc, r.sws, tie_count=ties)
+    r.sws.check()
+    tie_report = {"sampler_ratio_ties": int(ties[0]), "sampler_cdf_ties": int(ties[1]),
+                  "sampler_sequences": w.N, "selection": selection_tie_sample(w) if rank == 0 else None}
+    round_ms = pm["verify"] + pm["select"] + pm["draft"] + pm["sample"]
+    round_bytes = b["verify"] + b["select"] + sum(b["draft"]) + b["sample"]
+    extras = run_extras(args) if (rank == 0 and world == 1 and not args.no_extra) else None
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -509,7 +701,11 @@ def run_s3r(args, world, rank, local):
         "dense_decode_tokens_per_s": dense_tokens * world,
         "effective_tokens_per_s": eff_tokens * world,
         "mean_accepted_plus_one": mean_emitted,
-        "round_vs_dense_speedup": pm["dense"] / (pm["verify"] + pm["select"] + pm["draft"] + pm["sample"]),
+        "round_vs_dense_speedup": pm["dense"] / round_ms,
+        "s3r_round_gbs": gbs(round_bytes, round_ms),
+        "s3r_round_pct_of_8tbs": 100.0 * gbs(round_bytes, round_ms) / NOMINAL_HBM_GBS,
+        "emitted_tokens_speedup": (w.S * mean_emitted / round_ms) / (w.S * k / pm["dense"]),
+        "ties": tie_report,
         "phases": phases,
         "roofline": {"kernel": "attn_partial_kernel (dense decode)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -520,10 +716,15 @@ def run_s3r(args, world, rank, local):
         "e2e": e2e,
         "clocks": clock_info,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb, ct, desc = oracle_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": cb / ct / 1e9, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                "sample": desc + " (%.1f s)" % ct}
+    if extras is not None:
+        line["other_workloads"] = extras
+    if farm is not None:
+        try:
+            cb, ct, passes = farm.run(args.cpu_seconds)
+        finally:
+            farm.close()
+        line["cpu_baseline"] = {"value": cb / ct / 1e9, "unit": UNIT, "cores": farm.workers,
+                                "cpu_count": farm.cpu_count, "kind": "oracle", "sample": farm.describe(passes, ct)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -760,21 +961,27 @@ def run_sweep(args):
 
 def run_sampler(args):
     """Exact speculative sampling at rollout scale: 2048 sequences (256 prompts
-    x 8 responses) x k = 8 over V = 151936, sigma in {0.3, 1.0}."""
+    x 8 responses) x k = 8 over V = 151936, sigma in {0.3, 1.0} (the recipe)
+    and {0.12, 0.5} (the levels that give the ~95% and ~80% per-position
+    acceptance the workload aims for).  Per sigma: the parallel and the
+    sequential sampler, the acceptance and the sampler's tie counts."""
     import speculative_decode_attention_paged_b300 as s3r
     dev = torch.device("cuda", torch.cuda.current_device())
     sc = SAMPLER_ROLLOUT_2048SEQ
     N = args.seqs or sc.num_seqs
     res = {}
-    for sigma in sc.q_sigmas:
+    for sigma in tuple(sc.q_sigmas) + tuple(ROLLOUT_ACCEPTANCE_MATCHED_SIGMAS):
         inp = make_spec_inputs(N, sc.k, sc.vocab, sc.p_sigma, sigma, sc.seed, device=dev)
         ws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(N, sc.k), device=dev)
         out = torch.empty((N, sc.k + 1), dtype=torch.int32, device=dev)
         nacc = torch.empty((N,), dtype=torch.int32, device=dev)
+        ties = torch.zeros((2,), dtype=torch.int32, device=dev)
         clocks = _clock_sampler()
         t = _timed(lambda: s3r.s3r_spec_sample(inp.p_logits, inp.q_logits, inp.draft_tokens, sc.philox_seed, 0,
                                                out, nacc, ws), args.steps, args.warmup)
         clock_info = clocks.stop()
+        s3r.s3r_spec_sample(inp.p_logits, inp.q_logits, inp.draft_tokens, sc.philox_seed, 0, out, nacc, ws,
+                            tie_count=ties)
         ws.check()
         a = nacc.cpu().numpy()
         nbytes = N * (2 * sc.k + 1) * sc.vocab * 4 + N * (2 * sc.k + 2) * 4
@@ -795,6 +1002,8 @@ def run_sampler(args):
                       "gb": seq_bytes / 1e9, "gbs": seq_bytes / (t_seq * 1e-3) / 1e9,
                       "speedup_vs_parallel": t / t_seq}
         res[str(sigma)] = {"ms": t, "gb": nbytes / 1e9, "gbs": nbytes / (t * 1e-3) / 1e9,
+                           "recipe": "matched acceptance" if sigma in ROLLOUT_ACCEPTANCE_MATCHED_SIGMAS else "as written",
+                           "ratio_ties": int(ties[0]), "cdf_ties": int(ties[1]),
                            "sequential": sequential,
                            "mean_accepted": float(a.mean()), "mean_emitted": float((a + 1).mean()),
                            "per_position_acceptance": [float(x) for x in accepted / np.maximum(reached, 1)],
@@ -818,12 +1027,12 @@ def run_sampler(args):
             "draft_token_sampling": draft}
 
 
-def run_layers(args):
+class LayersRound:
     """Closed multi-layer S³R round: all 28 layers of the Qwen3-1.7B attention
     geometry, 32 sequences with histories U{4096..16384} in a pool sized for
     16K tokens per sequence (~60 GB), per-layer random queries and K/V rows,
     budget 0.05, k = 4, synthetic logits over V = 151936 (p ~ N(0, 3^2),
-    q = p + N(0, 1)).  One round, captured in one CUDA graph:
+    q = p + N(0, 1)).  One round (s3r_round), captured in one CUDA graph:
       4 draft steps: every layer writes its draft row at L + j and runs sparse
         draft attention over the previous round's pages, in one launch; the
         draft token is sampled from q_j in place;
@@ -832,115 +1041,147 @@ def run_layers(args):
         mass;
       exact speculative sampling of the 32 blocks, the length commit
         L' = L + n_acc + 1, and every layer's pages for the next round over L'.
-    Compared with 4 dense decode steps (a second graph): every layer writes
-    the step's row and runs dense attention in one launch, then a token is
-    sampled from p_j.
-    Both graphs restart from the same L at every replay (the appends rewrite
-    the same slots), so each timed step is the same round."""
-    import speculative_decode_attention_paged_b300 as s3r
-    dev = torch.device("cuda", torch.cuda.current_device())
-    c = ATTN_QWEN3_1P7B_28LAYER
-    sc = SAMPLER_ROUND_256SEQ
-    S, k, Hq, Hkv, n_layers = (args.seqs or c.num_seqs), c.k, c.q_heads, c.kv_heads, c.layers
-    if args.layers:
-        n_layers = args.layers
-    budget, V = c.budgets[0], sc.vocab
-    gen = torch.Generator(device="cpu")
-    gen.manual_seed(c.seed)
-    L = torch.randint(c.hist_min, c.hist_max + 1, (S,), generator=gen).to(torch.int32)
-    if args.all_16k:
-        L = torch.full((S,), c.capacity_tokens - 2 * k, dtype=torch.int32)
-    rows_gen = torch.Generator(device=dev)
-    rows_gen.manual_seed(c.seed + 1)
+    Compared with 4 dense decode steps (dense_steps, a second graph): every
+    layer writes the step's row and runs dense attention in one launch, then a
+    token is sampled from p_j.
+    Both restart from the same L at every replay (the appends rewrite the same
+    slots), so every replay is the same round.  The GPU parity test of this
+    workload replays the same graph and checks it against the oracle."""
 
-    def bf16_rows(*shape):
-        return (torch.randn(shape, generator=rows_gen, device=dev)).to(torch.bfloat16)
+    def __init__(self, dev, n_layers=None, num_seqs=None, all_16k=False):
+        import speculative_decode_attention_paged_b300 as s3r
+        self.s3r = s3r
+        c = ATTN_QWEN3_1P7B_28LAYER
+        sc = SAMPLER_ROUND_256SEQ
+        self.cfg, self.scfg = c, sc
+        S, k, Hq, Hkv = (num_seqs or c.num_seqs), c.k, c.q_heads, c.kv_heads
+        self.n_layers = n_layers or c.layers
+        self.S, self.k, self.Hq, self.Hkv = S, k, Hq, Hkv
+        self.budget, self.V = c.budgets[0], sc.vocab
+        self.all_16k = all_16k
+        gen = torch.Generator(device="cpu")
+        gen.manual_seed(c.seed)
+        L = torch.randint(c.hist_min, c.hist_max + 1, (S,), generator=gen).to(torch.int32)
+        if all_16k:
+            L = torch.full((S,), c.capacity_tokens - 2 * k, dtype=torch.int32)
+        self.L_host = L
+        rows_gen = torch.Generator(device=dev)
+        rows_gen.manual_seed(c.seed + 1)
 
-    layers = []
-    for li in range(n_layers):
-        kv = make_paged_kv(S, Hq, Hkv, 2 * k, seed=c.seed * 1000 + li, device=dev, hist_lens=L.to(dev),
-                           capacity_tokens=c.capacity_tokens)
-        desc = s3r.PagedKVDesc(kv.k_pool, kv.v_pool, kv.block_table, Hq)
-        b_max = selection_budget_pages(kv.max_pages, budget)
-        layers.append(dict(
-            kv=kv, desc=desc,
-            qv=make_queries(kv, 5000 + li, rows=k + 1), qd=[make_queries(kv, 5100 + 16 * li + j) for j in range(k)],
-            draft_kv=[(bf16_rows(S, 1, Hkv, 128), bf16_rows(S, 1, Hkv, 128)) for _ in range(k)],
-            block_kv=(bf16_rows(S, k + 1, Hkv, 128), bf16_rows(S, k + 1, Hkv, 128)),
-            out_v=torch.empty((S, k + 1, Hq, 128), dtype=torch.float32, device=dev),
-            out_d=[torch.empty((S, Hq, 128), dtype=torch.float32, device=dev) for _ in range(k)],
-            mass=torch.empty((S, Hkv, kv.max_pages), dtype=torch.float32, device=dev),
-            sel=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
-            cnt=torch.empty((S, Hkv), dtype=torch.int32, device=dev),
-            sel_next=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
-            cnt_next=torch.empty((S, Hkv), dtype=torch.int32, device=dev)))
-    max_len = layers[0]["kv"].max_pages * 16
-    spec = make_spec_inputs(S, k, V, sc.p_sigma, sc.q_sigmas[0], sc.seed, device=dev)
-    drafts = torch.empty((S, k), dtype=torch.int32, device=dev)
-    out_tokens = torch.empty((S, k + 1), dtype=torch.int32, device=dev)
-    n_acc = torch.empty((S,), dtype=torch.int32, device=dev)
-    dense_tokens = torch.empty((S, k), dtype=torch.int32, device=dev)
-    Ld = L.to(dev)
-    L_next = torch.empty_like(Ld)
-    ctx = [(Ld + j + 1).to(torch.int32) for j in range(k)]
-    ws = s3r.Workspace(s3r.s3r_attn_workspace_size(layers[0]["desc"], k + 1), device=dev)
-    sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(S, k), device=dev)
-    dws = s3r.Workspace(s3r.s3r_sample_draft_workspace_size(S), device=dev)
-    pool_gb = sum(2 * l["kv"].k_pool.numel() * 2 for l in layers) / 1e9
+        def bf16_rows(*shape):
+            return (torch.randn(shape, generator=rows_gen, device=dev)).to(torch.bfloat16)
 
-    def s3r_round():
+        self.layers = []
+        for li in range(self.n_layers):
+            kv = make_paged_kv(S, Hq, Hkv, 2 * k, seed=c.seed * 1000 + li, device=dev, hist_lens=L.to(dev),
+                               capacity_tokens=c.capacity_tokens)
+            desc = s3r.PagedKVDesc(kv.k_pool, kv.v_pool, kv.block_table, Hq)
+            b_max = selection_budget_pages(kv.max_pages, self.budget)
+            self.layers.append(dict(
+                kv=kv, desc=desc,
+                qv=make_queries(kv, 5000 + li, rows=k + 1),
+                qd=[make_queries(kv, 5100 + 16 * li + j) for j in range(k)],
+                draft_kv=[(bf16_rows(S, 1, Hkv, 128), bf16_rows(S, 1, Hkv, 128)) for _ in range(k)],
+                block_kv=(bf16_rows(S, k + 1, Hkv, 128), bf16_rows(S, k + 1, Hkv, 128)),
+                out_v=torch.empty((S, k + 1, Hq, 128), dtype=torch.float32, device=dev),
+                out_d=[torch.empty((S, Hq, 128), dtype=torch.float32, device=dev) for _ in range(k)],
+                mass=torch.empty((S, Hkv, kv.max_pages), dtype=torch.float32, device=dev),
+                sel=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
+                cnt=torch.empty((S, Hkv), dtype=torch.int32, device=dev),
+                sel_next=torch.empty((S, Hkv, b_max), dtype=torch.int32, device=dev),
+                cnt_next=torch.empty((S, Hkv), dtype=torch.int32, device=dev)))
+        self.max_len = self.layers[0]["kv"].max_pages * 16
+        self.spec = make_spec_inputs(S, k, self.V, sc.p_sigma, sc.q_sigmas[0], sc.seed, device=dev)
+        self.drafts = torch.empty((S, k), dtype=torch.int32, device=dev)
+        self.out_tokens = torch.empty((S, k + 1), dtype=torch.int32, device=dev)
+        self.n_acc = torch.empty((S,), dtype=torch.int32, device=dev)
+        self.dense_tokens = torch.empty((S, k), dtype=torch.int32, device=dev)
+        self.Ld = L.to(dev)
+        self.L_next = torch.empty_like(self.Ld)
+        self.ctx = [(self.Ld + j + 1).to(torch.int32) for j in range(k)]
+        self.ws = s3r.Workspace(s3r.s3r_attn_workspace_size(self.layers[0]["desc"], k + 1), device=dev)
+        self.sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(S, k), device=dev)
+        self.dws = s3r.Workspace(s3r.s3r_sample_draft_workspace_size(S), device=dev)
+        self.pool_gb = sum(2 * l["kv"].k_pool.numel() * 2 for l in self.layers) / 1e9
+        # the first round's pages: a verify of the block at L, selected over L + k (a previous round)
+        for l in self.layers:
+            s3r.s3r_kv_append(l["desc"], self.Ld, l["block_kv"][0], l["block_kv"][1], self.ws)
+            s3r.s3r_verify_attn(l["desc"], self.Ld, l["qv"], l["out_v"], 1.0, self.ws, page_mass=l["mass"])
+            s3r.s3r_select_draft_pages(l["mass"], (self.Ld + k).to(torch.int32), self.budget, l["sel"], l["cnt"],
+                                       self.ws)
+
+    def s3r_round(self):
+        s3r, sc, k = self.s3r, self.scfg, self.k
         for j in range(k):
-            for l in layers:
-                s3r.s3r_sparse_draft_attn(l["desc"], Ld, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0, ws,
-                                          append=l["draft_kv"][j])
-            s3r.s3r_sample_draft_tokens(spec.q_logits[:, j], sc.philox_seed, 0, j, drafts[:, j], dws)
-        for l in layers:
+            for l in self.layers:
+                s3r.s3r_sparse_draft_attn(l["desc"], self.Ld, j, l["sel"], l["cnt"], l["qd"][j], l["out_d"][j], 1.0,
+                                          self.ws, append=l["draft_kv"][j])
+            s3r.s3r_sample_draft_tokens(self.spec.q_logits[:, j], sc.philox_seed, 0, j, self.drafts[:, j], self.dws)
+        for l in self.layers:
             # the block's k + 1 rows by their own launch: timed in the round, this
             # beat the fused verify call (12.26 vs 12.34 ms at 28 layers)
-            s3r.s3r_kv_append(l["desc"], Ld, l["block_kv"][0], l["block_kv"][1], ws)
-            s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
-        s3r.s3r_spec_sample(spec.p_logits, spec.q_logits, drafts, sc.philox_seed, 0, out_tokens, n_acc, sws)
-        s3r.s3r_commit_lengths(Ld, n_acc, k, max_len, L_next, ws)
-        for l in layers:
-            s3r.s3r_select_draft_pages(l["mass"], L_next, budget, l["sel_next"], l["cnt_next"], ws)
+            s3r.s3r_kv_append(l["desc"], self.Ld, l["block_kv"][0], l["block_kv"][1], self.ws)
+            s3r.s3r_verify_attn(l["desc"], self.Ld, l["qv"], l["out_v"], 1.0, self.ws, page_mass=l["mass"])
+        s3r.s3r_spec_sample(self.spec.p_logits, self.spec.q_logits, self.drafts, sc.philox_seed, 0, self.out_tokens,
+                            self.n_acc, self.sws)
+        s3r.s3r_commit_lengths(self.Ld, self.n_acc, k, self.max_len, self.L_next, self.ws)
+        for l in self.layers:
+            s3r.s3r_select_draft_pages(l["mass"], self.L_next, self.budget, l["sel_next"], l["cnt_next"], self.ws)
 
-    def dense_steps():
-        for j in range(k):
-            for l in layers:
-                s3r.s3r_dense_decode_attn(l["desc"], ctx[j], l["qd"][j], l["out_d"][j], 1.0, ws,
+    def dense_steps(self):
+        s3r, sc = self.s3r, self.scfg
+        for j in range(self.k):
+            for l in self.layers:
+                s3r.s3r_dense_decode_attn(l["desc"], self.ctx[j], l["qd"][j], l["out_d"][j], 1.0, self.ws,
                                           append=l["draft_kv"][j])
-            s3r.s3r_sample_draft_tokens(spec.p_logits[:, j], sc.philox_seed, 0, j, dense_tokens[:, j], dws)
+            s3r.s3r_sample_draft_tokens(self.spec.p_logits[:, j], sc.philox_seed, 0, j, self.dense_tokens[:, j],
+                                        self.dws)
 
-    # the first round's pages: a verify of the block at L, selected over L + k (a previous round)
-    for l in layers:
-        s3r.s3r_kv_append(l["desc"], Ld, l["block_kv"][0], l["block_kv"][1], ws)
-        s3r.s3r_verify_attn(l["desc"], Ld, l["qv"], l["out_v"], 1.0, ws, page_mass=l["mass"])
-        s3r.s3r_select_draft_pages(l["mass"], (Ld + k).to(torch.int32), budget, l["sel"], l["cnt"], ws)
-    s3r_round()
-    dense_steps()
+    def check(self):
+        for w in (self.ws, self.sws, self.dws):
+            w.check()
+
+    def capture(self, dense=True):
+        """CUDA graphs of the round (and of the 4 dense steps); the calls
+        enqueue on torch's current stream, here a side stream under capture."""
+        g_round = torch.cuda.CUDAGraph()
+        g_dense = torch.cuda.CUDAGraph() if dense else None
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g_round, stream=side, capture_error_mode="thread_local"):
+                self.s3r_round()
+            if dense:
+                with torch.cuda.graph(g_dense, stream=side, capture_error_mode="thread_local"):
+                    self.dense_steps()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        return g_round, g_dense
+
+    def launches_per_round(self):
+        return self.n_layers * (self.k + 3) + self.k + 4 + 1
+
+
+def run_layers(args):
+    """The closed 28-layer round (LayersRound) against 4 dense decode steps,
+    both as CUDA graphs."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lr = LayersRound(dev, n_layers=args.layers, num_seqs=args.seqs, all_16k=args.all_16k)
+    S, k, Hq, Hkv, n_layers, V = lr.S, lr.k, lr.Hq, lr.Hkv, lr.n_layers, lr.V
+    L, Ld, layers = lr.L_host, lr.Ld, lr.layers
+    lr.s3r_round()
+    lr.dense_steps()
     torch.cuda.synchronize()
-    for w in (ws, sws, dws):
-        w.check()
-    # CUDA graphs: one per round, one per 4 dense steps (the calls enqueue on torch's current stream)
-    g_round, g_dense = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(g_round, stream=side, capture_error_mode="thread_local"):
-            s3r_round()
-        with torch.cuda.graph(g_dense, stream=side, capture_error_mode="thread_local"):
-            dense_steps()
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
+    lr.check()
+    g_round, g_dense = lr.capture()
     clocks = _clock_sampler()
     t_round = _timed(g_round.replay, args.steps, args.warmup)
     t_dense = _timed(g_dense.replay, args.steps, args.warmup)
-    t_round_eager = _timed(s3r_round, max(2, args.steps // 4), 1)
+    t_round_eager = _timed(lr.s3r_round, max(2, args.steps // 4), 1)
     clock_info = clocks.stop()
-    for w in (ws, sws, dws):
-        w.check()
-    a = n_acc.cpu().numpy().astype(np.int64)
-    if not np.array_equal(L_next.cpu().numpy(), L.numpy() + a + 1):
+    lr.check()
+    a = lr.n_acc.cpu().numpy().astype(np.int64)
+    if not np.array_equal(lr.L_next.cpu().numpy(), L.numpy() + a + 1):
         raise RuntimeError("length commit differs from L + n_acc + 1")
     Lsum = float(L.double().sum())
     tok = [sum(_visible_draft_tokens(l["sel"], l["cnt"], Ld, j) for l in layers) for j in range(k)]
@@ -955,8 +1196,8 @@ def run_layers(args):
     round_bytes = draft_bytes + verify_bytes + append_bytes + sample_bytes
     emitted = float((a + 1).sum())
     return {"workload": f"qwen3-1.7b-geom {n_layers} layers: {S} seqs x "
-                        + ("all 16K" if args.all_16k else "U{4096..16384}") + f" in a {pool_gb:.1f} GB pool, "
-                        f"budget {budget}, k={k}, verify k+1 rows, V={V} (sigma {sc.q_sigmas[0]}); "
+                        + ("all 16K" if args.all_16k else "U{4096..16384}") + f" in a {lr.pool_gb:.1f} GB pool, "
+                        f"budget {lr.budget}, k={k}, verify k+1 rows, V={V} (sigma {lr.scfg.q_sigmas[0]}); "
                         "closed round in one CUDA graph",
             "metric": METRIC, "value": round_bytes / (t_round * 1e-3) / 1e9, "unit": UNIT,
             "round_ms": t_round, "round_ms_eager": t_round_eager, "round_gb": round_bytes / 1e9,
@@ -967,7 +1208,7 @@ def run_layers(args):
             "s3r_emitted_tokens_per_s": emitted / (t_round * 1e-3),
             "dense_emitted_tokens_per_s": S * k / (t_dense * 1e-3),
             "emitted_tokens_speedup": (emitted / t_round) / (S * k / t_dense),
-            "launches_per_round": n_layers * (k + 3) + k + 4 + 1,
+            "launches_per_round": lr.launches_per_round(),
             "launches_per_dense_4_steps": k * (n_layers + 1), "clocks": clock_info}
 
 
@@ -1162,10 +1403,15 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("s3r", "reference"), default="s3r")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-workers", type=int, default=None,
+                    help="oracle processes for the CPU baseline (default: one per host core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=("round", "sweep", "sampler", "layers", "scheduler", "speedup"),
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave the other workloads' compact results out of the default line")
+    ap.add_argument("--workload", choices=("round", "tiny", "sweep", "sampler", "layers", "scheduler", "speedup"),
                     default="round",
-                    help="round (default): the 256-sequence S3R round + dense baseline; sweep: Qwen3-8B "
+                    help="round (default): the 256-sequence S3R round + dense baseline, with compact results of "
+                         "tiny, sweep, sampler and layers; tiny: 4 x 2048 latency per call; sweep: Qwen3-8B "
                          "geometry budget sweep; sampler: 2048 x k=8 sampler; layers: the 28-layer closed round; "
                          "scheduler: the AIMD KV scheduler simulation (host); speedup: the speedup-model "
                          "calibration on measured round and dense-step times")
@@ -1183,7 +1429,7 @@ def main(argv=None):
         if args.workload != "round":
             import speculative_decode_attention_paged_b300 as s3r
             s3r.load_library()
-            leg = {"sweep": run_sweep, "sampler": run_sampler, "layers": run_layers,
+            leg = {"tiny": run_tiny, "sweep": run_sweep, "sampler": run_sampler, "layers": run_layers,
                    "scheduler": run_scheduler, "speedup": run_speedup}[args.workload]
             line = leg(args)
             line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",

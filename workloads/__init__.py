@@ -7,8 +7,8 @@ arithmetic.
 """
 
 from .configs import (ATTN_CONFIGS, ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_1P7B_28LAYER, ATTN_QWEN3_8B_128SEQ,
-                      ATTN_TINY, SAMPLER_CONFIGS, SAMPLER_ROLLOUT_2048SEQ, SAMPLER_ROUND_256SEQ, SAMPLER_TINY,
-                      AttnConfig, SamplerConfig)
+                      ATTN_TINY, ROLLOUT_ACCEPTANCE_MATCHED_SIGMAS, SAMPLER_CONFIGS, SAMPLER_ROLLOUT_2048SEQ,
+                      SAMPLER_ROUND_256SEQ, SAMPLER_TINY, AttnConfig, SamplerConfig)
 from .attention_inputs import PagedKV, make_paged_kv, make_queries, bf16_to_bits
 from .sampler_inputs import SpecInputs, make_spec_inputs
 from .scheduler_inputs import RolloutRequests, make_rollout_requests
@@ -23,6 +23,7 @@ __all__ = [
     "SAMPLER_TINY",
     "SAMPLER_ROUND_256SEQ",
     "SAMPLER_ROLLOUT_2048SEQ",
+    "ROLLOUT_ACCEPTANCE_MATCHED_SIGMAS",
     "AttnConfig",
     "SamplerConfig",
     "PagedKV",

@@ -61,6 +61,10 @@ SAMPLER_ROUND_256SEQ = SamplerConfig("round-256seq-k4-v151936", num_seqs=256, k=
                                      q_sigmas=(1.0,), seed=2)
 SAMPLER_ROLLOUT_2048SEQ = SamplerConfig("rollout-2048seq-k8-v151936", num_seqs=2048, k=8, vocab=151936,
                                         p_sigma=3.0, q_sigmas=(0.3, 1.0), seed=4)
+# Draft-noise levels at which this recipe gives the ~95% and ~80% per-position
+# acceptance the rollout workload aims for (sum_v min(p, q) = 0.951 and 0.806
+# over V = 151936, p ~ N(0, 3^2)); the recipe's own 0.3 and 1.0 give 0.88 and 0.62.
+ROLLOUT_ACCEPTANCE_MATCHED_SIGMAS = (0.12, 0.5)
 
 ATTN_CONFIGS = {c.name: c for c in (ATTN_TINY, ATTN_QWEN3_1P7B_256SEQ, ATTN_QWEN3_8B_128SEQ, ATTN_QWEN3_1P7B_28LAYER)}
 SAMPLER_CONFIGS = {c.name: c for c in (SAMPLER_TINY, SAMPLER_ROUND_256SEQ, SAMPLER_ROLLOUT_2048SEQ)}
