@@ -123,6 +123,7 @@ _SIG = {
                                               _I32, ctypes.c_float, _P, ctypes.c_size_t, _P]),
     "s3r_kv_append": (ctypes.c_int, [ctypes.POINTER(_PagedKV), _P, _P, _I32, _P, _P, _P, ctypes.c_size_t, _P]),
     "s3r_commit_lengths": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, ctypes.c_size_t, _P]),
+    "s3r_test_stall_next_verify": (None, []),
 }
 
 _lib = None

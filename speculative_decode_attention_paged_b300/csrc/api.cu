@@ -3,6 +3,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -11,6 +12,7 @@
 #include "s3r_device.cuh"
 #include "spec_sample.cuh"
 #include "kv_append.cuh"
+#include "../../include/s3r_testing.h"
 
 namespace s3r {
 
@@ -45,6 +47,8 @@ constexpr int kMaxSelectPages = 49152;
 
 int g_sm_count[kMaxDevices];
 std::once_flag g_encode_once;
+// s3r_test_stall_next_verify: armed for the next tcgen05 verify launch only.
+std::atomic<int> g_test_stall{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -228,6 +232,7 @@ s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, 
       verify_tc_smem_bytes(a.n_chunks) <= max_dynamic_smem()) {
     CUtensorMap qmap;
     if (!encode_query_map(&qmap, q, kv->num_seqs, T, kv->num_q_heads, G)) return S3R_ERR_CUDA;
+    a.test_stall = g_test_stall.exchange(0);
     return to_status(launch_verify_tc(kmap, vmap, qmap, a, sms, static_cast<cudaStream_t>(stream)));
   }
   return to_status(launch_attention(kmap, vmap, a, sms, static_cast<cudaStream_t>(stream)));
@@ -238,6 +243,8 @@ s3r_status run_attention(const s3r_paged_kv* kv, int mode, const int32_t* lens, 
 extern "C" {
 
 const char* s3r_version(void) { return "s3r-b300 0.1.0 (sm_103a)"; }
+
+void s3r_test_stall_next_verify(void) { g_test_stall.store(1); }
 
 const char* s3r_status_string(s3r_status status) {
   switch (status) {

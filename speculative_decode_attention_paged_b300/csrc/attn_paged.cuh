@@ -51,6 +51,10 @@ struct AttnArgs {
   int total_warps;
   int n_pairs;
   int n_chunks;
+  // Test of the bounded waits only (0 otherwise): the tcgen05 verify kernel's CTA 0
+  // loads no K for its first tile and never arrives on that tile's barrier, so the
+  // waits on it run out and the abort path runs (see s3r_test_stall_next_verify).
+  int test_stall;
 };
 
 struct AttnWorkspaceLayout {

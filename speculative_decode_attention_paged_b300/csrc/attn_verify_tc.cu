@@ -333,9 +333,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           m.start = pstart;
         }
         __syncwarp();
+        // test of the bounded waits: CTA 0's first tile gets no K and no arrival
+        const bool stall_k = a.test_stall != 0 && blockIdx.x == 0 && t == 0;
         if (pid == 0 && lane == 0) {
           mbar_arrive(&meta_full[t % kMetaSlots]);
-          mbar_arrive_expect_tx(&k_full[st], __popc(loadmask) * 2u * kHalfBytes);
+          if (!stall_k) mbar_arrive_expect_tx(&k_full[st], __popc(loadmask) * 2u * kHalfBytes);
         }
         __syncwarp();
         // appended block rows of this tile's pages, each written by the producer
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool mine = load && (lane % kTcProducers) == pid;
         uint8_t* dst = stages + static_cast<size_t>(st) * kTcStageBytes + lane * kHalfBytes;
         const int y = h * kPage;
-        if (mine) {
+        if (mine && !stall_k) {
           tma_load_3d(dst, &kmap, 0, y, en.phys, &k_full[st], policy);
           tma_load_3d(dst + kTcRegion, &kmap, 64, y, en.phys, &k_full[st], policy);
         }

@@ -1,5 +1,5 @@
-"""The C-ABI library loads, exports every entry point include/s3r.h declares,
-and rejects bad arguments on the host before touching a GPU."""
+"""The C-ABI library loads, exports every entry point the headers under
+include/ declare, and rejects bad arguments on the host before touching a GPU."""
 
 import ctypes
 import os
@@ -11,11 +11,12 @@ import speculative_decode_attention_paged_b300 as s3r
 from speculative_decode_attention_paged_b300 import build as s3r_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "s3r.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
 
 
 def _declared():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"S3R_API\s+[^;(]*?\b(s3r_\w+)\s*\(", text)))
 
 
@@ -28,7 +29,7 @@ def lib():
 def test_header_declares_the_entry_points():
     names = _declared()
     for want in ("s3r_dense_decode_attn", "s3r_sparse_draft_attn", "s3r_verify_attn",
-                 "s3r_select_draft_pages", "s3r_spec_sample"):
+                 "s3r_select_draft_pages", "s3r_spec_sample", "s3r_sched_run", "s3r_test_stall_next_verify"):
         assert want in names
 
 
