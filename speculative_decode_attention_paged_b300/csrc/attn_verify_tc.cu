@@ -597,17 +597,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         x[j] = fast_exp2(x[j] - mu[j]);
         l_part[j] += x[j];
       }
-      if (MASS) {
-        // per (page, row) log-sum-exp: sum over the 16 tokens of the page
-#pragma unroll
-        for (int j = 0; j < kRowsWg; ++j) v[j] = x[j];
-        reduce_scatter<16, kRowsWg, false>(v, lane);   // lane holds row (lane & 15)
-        const int r = r0 + (lane & 15);
-        if (page < n && r < a.R) {
-          a.page_lse[(static_cast<int64_t>(pair) * a.max_pages + e0 + page) * a.R + r] =
-              v[0] > 0.f ? m_lane + fast_log2(v[0]) : kNegInf;
-        }
-      }
       // P^T (bf16 high part and remainder); the buffer is free once PV(t-1) is done
       if (t > 0 && !waited_prev)
         ok_acc = ok_acc && wait_or_abort(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag, a.err);
@@ -625,6 +614,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      if (MASS) {
+        // per (page, row) log-sum-exp, after P^T is handed to the output MMA (it
+        // runs meanwhile): the sum over the 16 tokens of the page
+#pragma unroll
+        for (int j = 0; j < kRowsWg; ++j) v[j] = x[j];
+        reduce_scatter<16, kRowsWg, false>(v, lane);   // lane holds row (lane & 15)
+        const int r = r0 + (lane & 15);
+        if (page < n && r < a.R) {
+          a.page_lse[(static_cast<int64_t>(pair) * a.max_pages + e0 + page) * a.R + r] =
+              v[0] > 0.f ? m_lane + fast_log2(v[0]) : kNegInf;
+        }
+      }
 
       if (!(flags & kTileLast)) continue;
       // =========================== end of this pair's segment
