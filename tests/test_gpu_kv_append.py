@@ -171,6 +171,13 @@ def test_fused_append_equals_append_then_attend(mode, q_heads, T):
         from helpers import assert_attn_close
         ref = oracle.dense_decode_attn(bf16_to_bits(make_queries(fus, 70)), kp, vp, bt, host(fus.hist_lens) + 1, 1.0)
         assert_attn_close(outs[1], ref, "fused dense")
+    else:
+        # L = 15 and 17: the selected history page is also the draft tail's
+        # first page, so two entries of the stream write and read that page
+        from helpers import assert_attn_close
+        ref = oracle.sparse_draft_attn(bf16_to_bits(make_queries(fus, 71)), kp, vp, bt, host(fus.hist_lens), j,
+                                       host(sel), host(sel_cnt), 1.0)
+        assert_attn_close(outs[1], ref, "fused sparse")
 
 
 def test_fused_append_skips_rows_of_bad_pages():
