@@ -177,8 +177,8 @@ class Runner:
         dev = w.kv.k_pool.device
         self.ws = s3r.Workspace(s3r.s3r_attn_workspace_size(self.desc, w.k), device=dev)
         self.sws = s3r.Workspace(s3r.s3r_spec_sample_workspace_size(w.N, w.scfg.k), device=dev)
-        # dense x k, verify, select, drafts x k, sampler x 4 (one kernel per attention call)
-        self.launches_per_step = w.k + 1 + 1 + w.k + 4
+        # dense x k, verify, select, drafts x k, sampler (one kernel per call)
+        self.launches_per_step = w.k + 1 + 1 + w.k + 1
 
     def step(self, ev=None):
         """ev: list of 2k+4 events recorded at the phase boundaries, or None."""
@@ -1211,7 +1211,9 @@ class LayersRound:
         return g_round, g_dense
 
     def launches_per_round(self):
-        return self.n_layers * (self.k + 3) + self.k + 4 + 1
+        # per layer: k drafts, block append, verify, selection; then k draft-token samplings,
+        # the sampler and the length commit
+        return self.n_layers * (self.k + 3) + self.k + 1 + 1
 
 
 def run_layers(args):

@@ -399,7 +399,7 @@ S3R_API s3r_status s3r_commit_lengths(const int32_t* hist_lens, const int32_t* n
  *                 call's device error bits (the S3R_DEVERR_* values)
  * Returns S3R_ERR_UNSUPPORTED, before enqueuing anything, when
  * s3r_spec_sample_workspace_size(n, k) exceeds S3R_NOALLOC_SCRATCH_BYTES
- * (for example n = 2048 with k = 8 needs 1,868,032 bytes and fits).  Every
+ * (for example n = 2048 with k = 8 needs 1,884,672 bytes and fits).  Every
  * other argument error also returns before anything is enqueued.
  * The stream and every pointer must belong to the CURRENT device: the call
  * uses the current device's copy of the array.  The first call on each

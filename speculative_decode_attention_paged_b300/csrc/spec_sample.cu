@@ -7,23 +7,29 @@
 // from the residual distribution (rit.work, "Как разреженный черновик
 // сохраняет ответы плотной модели"; rebasdaily.com, "草稿可以稀疏，交卷必须完整").
 //
-// Kernels, all parallel over rows or chunks of rows.  Each row is cut into 32
-// contiguous chunks.
-//   row_stats   one CTA per logit row (k+1 target rows and k draft rows per
-//               sequence), one warp per chunk: the row max m and
-//               z = sum_v 2^((x_v - m) log2 e) in one streaming pass with
-//               16-byte loads; the bonus row p_k also keeps its 32 chunk
-//               (max, sum) pairs, which are its chunk masses;
-//   accept      one warp per sequence: the k ratio tests p_i(x_i)/q_i(x_i)
-//               against Philox uniforms (fp64 ratio from fp32 row stats);
-//               a = the first rejected position (k if none);
-//   chunk_sum   one CTA per (sequence, chunk) of a sequence that rejected:
-//               fp64 sums over the chunk of the residual max(0, p_a - q_a)
+// The steps, each parallel over rows or chunks of rows.  Each row is cut into
+// 32 contiguous chunks.
+//   row stats   one CTA per logit row (k+1 target rows and k draft rows per
+//               sequence): the row max m and z = sum_v 2^((x_v - m) log2 e)
+//               in one streaming pass with 16-byte loads; the bonus row p_k
+//               also keeps its 32 chunk (max, sum) pairs, which are its chunk
+//               masses;
+//   ratio tests one warp per sequence: the k tests p_i(x_i)/q_i(x_i) against
+//               Philox uniforms (fp64 ratio from fp32 row stats); a = the
+//               first rejected position (k if none);
+//   chunk sums  one CTA per (sequence, 8 chunks) of a sequence that rejected:
+//               fp64 sums over each chunk of the residual max(0, p_a - q_a)
 //               and of p_a (the fallback when the residual vanishes);
 //   pick        one CTA per sequence: the chunk masses locate the chunk
 //               holding u * Z; that chunk alone is scanned in token-id order
 //               (fp32 sums over contiguous per-thread runs, fp64 prefix across
 //               runs) to find the token.
+// The parallel sampler runs them all in one launch (spec_fused_kernel): CTAs
+// take tasks in ticket order, first every row of sequence 0, 1, ..., then the
+// chunk sums of each sequence; the last row of a sequence to finish runs its
+// ratio tests (and, if every draft was accepted, its bonus pick), and the last
+// of its chunk-sum tasks its pick.  A sequence's chunk sums so re-read p_a and
+// q_a while later sequences' rows still stream.
 // With k = 0 there is nothing to test and the row is its own bonus row:
 // bonus_sample streams each row with 4 CTAs, the last of which merges the
 // chunk statistics and picks the token.
@@ -168,28 +174,6 @@ __device__ __forceinline__ double chunk_mass(float2 c, float2 row) {
   return v > 0.0 ? v : 0.0;
 }
 
-// One CTA per logit row (k+1 target rows, then k draft rows per sequence):
-// the row's (max, sum) and, for the bonus row p_k, its 32 chunk statistics,
-// which give the bonus row's chunk masses without a second pass.
-template <bool VEC>
-__global__ void __launch_bounds__(kStatThreads)
-    row_stats_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
-                     float2* __restrict__ stats, float2* __restrict__ bonus_chunks) {
-  const int row = blockIdx.x;
-  const int np = N * (k + 1);
-  const float* x = row < np ? p + static_cast<int64_t>(row) * V
-                            : q + static_cast<int64_t>(row - np) * V;
-  __shared__ float2 s_c[kSampleChunks];
-  block_chunk_stats<VEC>(x, V, s_c);
-  if (threadIdx.x < 32) {
-    const float2 cs = s_c[threadIdx.x];
-    const float2 r = merge_chunk_stats(cs);
-    if (threadIdx.x == 0) stats[row] = r;
-    if (row < np && row % (k + 1) == k)
-      bonus_chunks[static_cast<int64_t>(row / (k + 1)) * kSampleChunks + threadIdx.x] = cs;
-  }
-}
-
 // The row a sequence samples from, in probability space: the residual
 // max(0, p(v) - q(v)) after a rejection, or p(v) itself for the bonus token
 // (q == null).  One inline definition, so every kernel computes the same values.
@@ -210,7 +194,7 @@ struct SampleRow {
 __device__ __forceinline__ SampleRow sample_row(const float* p, const float* q, const float2* stats,
                                                 int N, int k, int V, int n, int a, bool use_p) {
   SampleRow row;
-  const float2 sp = stats[static_cast<int64_t>(n) * (k + 1) + a];
+  const float2 sp = __ldcg(stats + static_cast<int64_t>(n) * (k + 1) + a);
   row.p = p + (static_cast<int64_t>(n) * (k + 1) + a) * V;
   row.mp = sp.x * kLog2e;
   row.izp = 1.f / sp.y;
@@ -218,7 +202,7 @@ __device__ __forceinline__ SampleRow sample_row(const float* p, const float* q, 
   row.mq = 0.f;
   row.izq = 0.f;
   if (a < k && !use_p) {
-    const float2 sq = stats[static_cast<int64_t>(N) * (k + 1) + static_cast<int64_t>(n) * k + a];
+    const float2 sq = __ldcg(stats + static_cast<int64_t>(N) * (k + 1) + static_cast<int64_t>(n) * k + a);
     row.q = q + (static_cast<int64_t>(n) * k + a) * V;
     row.mq = sq.x * kLog2e;
     row.izq = 1.f / sq.y;
@@ -248,15 +232,12 @@ __device__ __forceinline__ bool ratio_tie(double ratio, float u) {
 // (k if none), the accepted drafts and the -1 padding after position a.  With
 // ties != null, ties[0] gains the number of tests up to and including the
 // first rejection whose uniform lies within kRatioTie of the ratio.
-__global__ void __launch_bounds__(256)
-    accept_kernel(const float* __restrict__ p, const float* __restrict__ q,
-                  const int32_t* __restrict__ drafts, int N, int k, int V, uint64_t seed,
-                  uint32_t offset, const float2* __restrict__ stats, int32_t* __restrict__ accept,
-                  int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err,
-                  uint32_t* __restrict__ ties) {
-  const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (n >= N) return;
+__device__ __forceinline__ int accept_sequence(const float* __restrict__ p, const float* __restrict__ q,
+                                               const int32_t* __restrict__ drafts, int N, int k, int V,
+                                               uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
+                                               int32_t* __restrict__ accept, int32_t* __restrict__ out_tokens,
+                                               int32_t* __restrict__ n_accepted, int* err,
+                                               uint32_t* __restrict__ ties, int n, int lane) {
   const int np_rows = N * (k + 1);
   int first = k;
   uint64_t tie_bits = 0;   // bit i: test i is a tie (k <= 64)
@@ -271,8 +252,8 @@ __global__ void __launch_bounds__(256)
       } else {
         const double ratio = draft_ratio(__ldg(p + (static_cast<int64_t>(n) * (k + 1) + i) * V + x),
                                          __ldg(q + (static_cast<int64_t>(n) * k + i) * V + x),
-                                         stats[static_cast<int64_t>(n) * (k + 1) + i],
-                                         stats[np_rows + static_cast<int64_t>(n) * k + i]);
+                                         __ldcg(stats + static_cast<int64_t>(n) * (k + 1) + i),
+                                         __ldcg(stats + np_rows + static_cast<int64_t>(n) * k + i));
         const float u = philox_uniform(seed, offset, n, i, kStreamAccept);
         rej = ratio_rejects(ratio, u);
         tie = ratio_tie(ratio, u);
@@ -296,6 +277,7 @@ __global__ void __launch_bounds__(256)
     accept[n] = first;
     n_accepted[n] = first;
   }
+  return first;
 }
 
 // s += x with Kahan compensation c (the sum is s - c).
@@ -314,14 +296,9 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 // p_k, whose chunk masses the row statistics already hold: their CTAs return
 // at once.  Coalesced 16-byte loads.
 template <bool VEC>
-__global__ void __launch_bounds__(kStatThreads)
-    chunk_sum_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
-                     const float2* __restrict__ stats, const int32_t* __restrict__ accept,
-                     double2* __restrict__ chunk_sums) {
-  const int n = blockIdx.x / kRowParts;
-  const int part = blockIdx.x - n * kRowParts;
-  const int a = __ldg(accept + n);
-  if (a == k) return;
+__device__ __forceinline__ void residual_chunk_sums(const float* __restrict__ p, const float* __restrict__ q,
+                                                   int N, int k, int V, const float2* __restrict__ stats,
+                                                   double2* __restrict__ chunk_sums, int n, int part, int a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SampleRow row = sample_row(p, q, stats, N, k, V, n, a, false);
   const int CL = chunk_len(V);
@@ -377,6 +354,18 @@ __global__ void __launch_bounds__(kStatThreads)
     dp += __shfl_xor_sync(0xffffffffu, dp, o);
   }
   if (lane == 0) chunk_sums[static_cast<int64_t>(n) * kSampleChunks + c] = make_double2(dr, dp);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kStatThreads)
+    chunk_sum_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
+                     const float2* __restrict__ stats, const int32_t* __restrict__ accept,
+                     double2* __restrict__ chunk_sums) {
+  const int n = blockIdx.x / kRowParts;
+  const int part = blockIdx.x - n * kRowParts;
+  const int a = __ldg(accept + n);
+  if (a == k) return;
+  residual_chunk_sums<VEC>(p, q, N, k, V, stats, chunk_sums, n, part, a);
 }
 
 // Warp-wide, lane c holding chunk c's mass v >= 0 (fp64): the chunk where the
@@ -489,26 +478,26 @@ __device__ __forceinline__ int block_pick_in_chunk(const SampleRow& row, int lo,
 // residual's, or p_a's when the residual vanishes, or the bonus row's from its
 // chunk statistics) locate the chunk holding u * Z; that chunk is scanned in
 // token-id order.
-__global__ void __launch_bounds__(kPickThreads)
-    pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
-                uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
-                const float2* __restrict__ bonus_chunks, const int32_t* __restrict__ accept,
-                const double2* __restrict__ chunk_sums, int32_t* __restrict__ out_tokens,
-                uint32_t* __restrict__ ties) {
+// Block-wide (every thread of the CTA): sequence n's token at position a.
+__device__ __forceinline__ void pick_sequence(const float* __restrict__ p, const float* __restrict__ q, int N,
+                                              int k, int V, uint64_t seed, uint32_t offset,
+                                              const float2* __restrict__ stats,
+                                              const float2* __restrict__ bonus_chunks, int a,
+                                              const double2* __restrict__ chunk_sums,
+                                              int32_t* __restrict__ out_tokens, uint32_t* __restrict__ ties,
+                                              int n) {
   __shared__ PickSmem sm;
   __shared__ int s_chunk, s_use_p;
   __shared__ double s_tgt, s_eps;
-  const int n = blockIdx.x;
   const int tid = threadIdx.x;
-  const int a = __ldg(accept + n);
   if (tid < 32) {
     double2 cs;
     if (a == k) {
-      const double v = chunk_mass(bonus_chunks[static_cast<int64_t>(n) * kSampleChunks + tid],
-                                  stats[static_cast<int64_t>(n) * (k + 1) + k]);
+      const double v = chunk_mass(__ldcg(bonus_chunks + static_cast<int64_t>(n) * kSampleChunks + tid),
+                                  __ldcg(stats + static_cast<int64_t>(n) * (k + 1) + k));
       cs = make_double2(v, v);
     } else {
-      cs = chunk_sums[static_cast<int64_t>(n) * kSampleChunks + tid];
+      cs = __ldcg(chunk_sums + static_cast<int64_t>(n) * kSampleChunks + tid);
     }
     double zr = cs.x;
 #pragma unroll
@@ -537,6 +526,17 @@ __global__ void __launch_bounds__(kPickThreads)
     out_tokens[static_cast<int64_t>(n) * (k + 1) + a] = tok;
     if (ties != nullptr && sm.tie) atomicAdd(ties + 1, 1u);
   }
+}
+
+__global__ void __launch_bounds__(kPickThreads)
+    pick_kernel(const float* __restrict__ p, const float* __restrict__ q, int N, int k, int V,
+                uint64_t seed, uint32_t offset, const float2* __restrict__ stats,
+                const float2* __restrict__ bonus_chunks, const int32_t* __restrict__ accept,
+                const double2* __restrict__ chunk_sums, int32_t* __restrict__ out_tokens,
+                uint32_t* __restrict__ ties) {
+  const int n = blockIdx.x;
+  pick_sequence(p, q, N, k, V, seed, offset, stats, bonus_chunks, __ldg(accept + n), chunk_sums, out_tokens, ties,
+                n);
 }
 
 // Rows split over CTAs: each of kRowParts CTAs streams 8 chunks of a row (one
@@ -692,6 +692,120 @@ __global__ void __launch_bounds__(kStatThreads)
   }
 }
 
+__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* ptr, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// The parallel sampler in one launch.  Each CTA takes a ticket; tickets
+// [0, N(2k+1)) are the rows, sequence-major (p_0..p_k, then q_0..q_{k-1} of
+// sequence 0, then of sequence 1, ...), and the next N * kRowParts tickets the
+// chunk-sum tasks of sequence 0, 1, ....  Row task: the row's statistics (and
+// the bonus row's chunk statistics); the last of a sequence's 2k+1 rows to
+// finish runs the ratio tests, picks the bonus token if every draft was
+// accepted, and marks the sequence ready.  Chunk-sum task: waits until its
+// sequence is ready -- every row task holds a lower ticket, so it has started
+// and waits on nothing, and the wait ends -- then sums its 8 chunks of the
+// residual row a (nothing if a == k); the last of the sequence's tasks picks
+// the token and clears the sequence's counters.  The last CTA to finish clears
+// the ticket.  The arithmetic of every step is that of the separate kernels.
+template <bool VEC>
+__global__ void __launch_bounds__(kStatThreads)
+    spec_fused_kernel(const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ drafts,
+                      int N, int k, int V, uint64_t seed, uint32_t offset, float2* __restrict__ stats,
+                      float2* __restrict__ bonus, int32_t* __restrict__ accept, double2* __restrict__ chunk_sums,
+                      int32_t* __restrict__ out_tokens, int32_t* __restrict__ n_accepted, int* err,
+                      uint32_t* __restrict__ ties, int* __restrict__ row_arrive, int* __restrict__ res_arrive,
+                      int* __restrict__ ready, int* __restrict__ ticket) {
+  __shared__ int s_task, s_flag, s_first;
+  __shared__ float2 s_c[kSampleChunks];
+  const int tid = threadIdx.x;
+  if (tid == 0) s_task = atomicAdd(ticket, 1);
+  __syncthreads();
+  const int task = s_task;
+  const int R = 2 * k + 1;
+  const int row_tasks = N * R;
+  if (task < row_tasks) {
+    const int n = task / R, r = task - (task / R) * R;
+    const bool is_p = r <= k;
+    const int64_t row = is_p ? static_cast<int64_t>(n) * (k + 1) + r
+                             : static_cast<int64_t>(N) * (k + 1) + static_cast<int64_t>(n) * k + (r - k - 1);
+    const float* x = is_p ? p + (static_cast<int64_t>(n) * (k + 1) + r) * V
+                          : q + (static_cast<int64_t>(n) * k + (r - k - 1)) * V;
+    block_chunk_stats<VEC>(x, V, s_c);
+    if (tid < 32) {
+      const float2 cs = s_c[tid];
+      const float2 rr = merge_chunk_stats(cs);
+      if (tid == 0) stats[row] = rr;
+      if (r == k) bonus[static_cast<int64_t>(n) * kSampleChunks + tid] = cs;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      fence_acq_rel_gpu();
+      s_flag = atomicAdd(row_arrive + n, 1) == R - 1;
+    }
+    __syncthreads();
+    if (s_flag) {
+      fence_acq_rel_gpu();
+      if (tid < 32) {
+        const int first = accept_sequence(p, q, drafts, N, k, V, seed, offset, stats, accept, out_tokens,
+                                          n_accepted, err, ties, n, tid);
+        if (tid == 0) s_first = first;
+      }
+      __syncthreads();
+      if (s_first == k) pick_sequence(p, q, N, k, V, seed, offset, stats, bonus, k, chunk_sums, out_tokens, ties, n);
+      if (tid == 0) {
+        row_arrive[n] = 0;
+        fence_acq_rel_gpu();
+        st_release_gpu(ready + n, 1);
+      }
+    }
+  } else {
+    const int rt = task - row_tasks;
+    const int n = rt / kRowParts, part = rt - (rt / kRowParts) * kRowParts;
+    if (tid == 0) {
+      int ok = 0;
+      for (uint32_t i = 0; i < kMaxSpin; ++i) {
+        if (ld_acquire_gpu(ready + n) != 0) {
+          ok = 1;
+          break;
+        }
+        __nanosleep(256);
+      }
+      if (!ok) report_error(err, S3R_DEVERR_TIMEOUT);
+      s_flag = ok;
+    }
+    __syncthreads();
+    const int ok = s_flag;
+    fence_acq_rel_gpu();
+    const int a = ok ? __ldcg(accept + n) : k;
+    if (a < k) residual_chunk_sums<VEC>(p, q, N, k, V, stats, chunk_sums, n, part, a);
+    __syncthreads();
+    if (tid == 0) {
+      fence_acq_rel_gpu();
+      s_flag = atomicAdd(res_arrive + n, 1) == kRowParts - 1;
+    }
+    __syncthreads();
+    if (s_flag) {
+      fence_acq_rel_gpu();
+      if (a < k) pick_sequence(p, q, N, k, V, seed, offset, stats, bonus, a, chunk_sums, out_tokens, ties, n);
+      if (tid == 0) {
+        res_arrive[n] = 0;
+        ready[n] = 0;
+      }
+    }
+  }
+  if (tid == 0 && atomicAdd(ticket + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+    ticket[0] = 0;
+    ticket[1] = 0;
+  }
+}
+
 // chunk_sum then pick, after the ratio tests have set accept[] and the stats.
 cudaError_t launch_residual_pick(const float* p, const float* q, int N, int k, int V, uint64_t seed,
                                  uint32_t offset, const float2* stats, const float2* bonus,
@@ -721,7 +835,10 @@ SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k) {
   L.chunk_off = L.accept_off + al(static_cast<size_t>(N) * sizeof(int32_t));
   L.bonus_off = L.chunk_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(double2));
   L.arrive_off = L.bonus_off + al(static_cast<size_t>(N) * kSampleChunks * sizeof(float2));
-  L.total = L.arrive_off + al(static_cast<size_t>(N) * sizeof(int));
+  L.res_arrive_off = L.arrive_off + static_cast<size_t>(N) * sizeof(int);
+  L.ready_off = L.res_arrive_off + static_cast<size_t>(N) * sizeof(int);
+  L.ticket_off = L.ready_off + static_cast<size_t>(N) * sizeof(int);
+  L.total = al(L.ticket_off + 2 * sizeof(int));
   return L;
 }
 
@@ -757,20 +874,20 @@ cudaError_t launch_spec_sample(const float* p, const float* q, const int32_t* dr
     }
     return cudaGetLastError();
   }
-  const int rows = N * (2 * k + 1);
+  int* res_arrive = reinterpret_cast<int*>(w + L.res_arrive_off);
+  int* ready = reinterpret_cast<int*>(w + L.ready_off);
+  int* ticket = reinterpret_cast<int*>(w + L.ticket_off);
+  const unsigned blocks = static_cast<unsigned>(static_cast<int64_t>(N) * (2 * k + 1 + kRowParts));
   if (vec) {
-    row_stats_kernel<true><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, bonus);
+    spec_fused_kernel<true><<<blocks, kStatThreads, 0, stream>>>(p, q, drafts, N, k, V, seed, offset, stats, bonus,
+                                                                 accept, chunks, out_tokens, n_accepted, err, ties,
+                                                                 arrivals, res_arrive, ready, ticket);
   } else {
-    row_stats_kernel<false><<<rows, kStatThreads, 0, stream>>>(p, q, N, k, V, stats, bonus);
+    spec_fused_kernel<false><<<blocks, kStatThreads, 0, stream>>>(p, q, drafts, N, k, V, seed, offset, stats,
+                                                                  bonus, accept, chunks, out_tokens, n_accepted, err,
+                                                                  ties, arrivals, res_arrive, ready, ticket);
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  accept_kernel<<<(N + 7) / 8, 256, 0, stream>>>(p, q, drafts, N, k, V, seed, offset, stats, accept,
-                                                  out_tokens, n_accepted, err, ties);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_residual_pick(p, q, N, k, V, seed, offset, stats, bonus, accept, chunks, out_tokens, vec, ties,
-                              stream);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_spec_sample_sequential(const float* p, const float* q, const int32_t* drafts, int N, int k,

@@ -22,8 +22,11 @@ struct SpecWorkspaceLayout {
   size_t accept_off;  // int32 [N]: accepted count a = index of the row sampled from
   size_t chunk_off;   // double2 [N][kSampleChunks]: (residual sum, target-row sum) per chunk
   size_t bonus_off;   // float2 [N][kSampleChunks]: (max, sum) per chunk of the bonus row p_k
-  size_t arrive_off;  // int32 [N]: per-sequence arrival counters, zero between calls
-  size_t total;
+  size_t arrive_off;      // int32 [N]: per-sequence arrival counters, zero between calls
+  size_t res_arrive_off;  // int32 [N]: per-sequence chunk-sum arrivals, zero between calls
+  size_t ready_off;       // int32 [N]: per-sequence "ratio tests done" flags, zero between calls
+  size_t ticket_off;      // int32 [2]: task ticket and finished-CTA count, zero between calls
+  size_t total;           // the counters [arrive_off, total) are contiguous
 };
 
 SpecWorkspaceLayout spec_workspace_layout(int64_t N, int k);

@@ -4,11 +4,11 @@
 // Some callers have no way to allocate a workspace: code running inside a
 // memory pool that is fully reserved up front, plugins handed only their
 // input and output buffers, or drivers that forbid cudaMalloc after start-up.
-// This entry point runs the same sampler kernels as s3r_spec_sample (row
-// statistics, ratio tests, residual chunk sums and the inverse-CDF pick; for
-// k = 0 the one-pass bonus sampler), with their scratch (the error word, the
-// per-row statistics and the per-sequence arrival counters) in a fixed-size
-// array that lives in the library's own device image.  The array exists once
+// This entry point runs the same sampler as s3r_spec_sample (row statistics,
+// ratio tests, residual chunk sums and the inverse-CDF pick in one launch; for
+// k = 0 the one-pass bonus sampler), with its scratch (the error word, the
+// per-row statistics, the per-sequence counters and the task ticket) in a
+// fixed-size array that lives in the library's own device image.  The array exists once
 // per GPU that loads the library and stays allocated until the process exits.
 //
 // The array is a __device__ symbol: in host code its name is only a host-side
@@ -76,13 +76,14 @@ extern "C" s3r_status s3r_spec_sample_noalloc(const float* p_logits, const float
   void* ws = scratch_address(dev);
   if (ws == nullptr) return S3R_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: clear the error word, and
-  // for k = 0 the per-sequence arrival counters that sampler counts on.
+  // The array keeps the previous call's contents: clear the error word and
+  // the counters the sampler's kernels count on (per-sequence arrivals and
+  // flags, the task ticket), which a call that stopped on a device error may
+  // have left set.
   if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return forget_on_failure(dev, S3R_ERR_CUDA);
-  if (k == 0 && n > 0) {
+  if (n > 0) {
     const s3r::SpecWorkspaceLayout L = s3r::spec_workspace_layout(n, k);
-    if (cudaMemsetAsync(static_cast<unsigned char*>(ws) + L.arrive_off, 0, static_cast<size_t>(n) * sizeof(int),
-                        s) != cudaSuccess)
+    if (cudaMemsetAsync(static_cast<unsigned char*>(ws) + L.arrive_off, 0, L.total - L.arrive_off, s) != cudaSuccess)
       return forget_on_failure(dev, S3R_ERR_CUDA);
   }
   st = s3r_spec_sample(p_logits, q_logits, draft_tokens, n, k, vocab, seed, offset, out_tokens, n_accepted,
