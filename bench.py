@@ -800,7 +800,7 @@ def measured_peaks(root=None):
 # 32-sequence case of this workload; traffic grows with the KV streamed, so the
 # full launch's traffic is this ratio times its algorithmic bytes.  None when
 # the kernel has changed since the capture.
-DENSE_TRAFFIC_RATIO = (1348025856 + 2904832) / 1346994176
+DENSE_TRAFFIC_RATIO = (1348030976 + 2870784) / 1346994176
 
 
 def _mirror(w):

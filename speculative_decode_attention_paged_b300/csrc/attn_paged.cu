@@ -20,7 +20,7 @@
 //     writer publishes its segment with a fence and an arrival counter, and
 //     the last segment to arrive merges them (log-sum-exp merge) in place, so
 //     one launch does the whole call.
-//   * Each warp runs its own 3-stage TMA pipeline (cp.async.bulk.tensor, one
+//   * Each warp runs its own 2-stage TMA pipeline (cp.async.bulk.tensor, one
 //     mbarrier per stage, 128-byte swizzle so ldmatrix reads are
 //     bank-conflict free).  Page ids are fetched 32 at a time, one per lane.
 //   * The G (decode / draft) or T*G (verify) query rows of a pair share every

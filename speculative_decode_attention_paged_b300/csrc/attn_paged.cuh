@@ -14,7 +14,10 @@ namespace s3r {
 enum AttnMode : int { kModeDense = 0, kModeSparse = 1, kModeVerify = 2 };
 
 constexpr int kAttnWarps = 8;       // warps per CTA, each an independent worker
-constexpr int kAttnStages = 3;      // TMA stages per warp (one (page, KV head) K+V tile each)
+// TMA stages per warp (one (page, KV head) K+V tile each): two stages (128 KiB
+// in flight per SM) stream faster than three (192 KiB), which only queue
+// longer in DRAM.
+constexpr int kAttnStages = 2;
 constexpr int kPairChunk = 32;      // (sequence, KV head) pairs per prefix-sum chunk
 constexpr int kMaxPairs = 262144;   // chunk prefix must fit in shared memory
 
