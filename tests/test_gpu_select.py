@@ -29,10 +29,12 @@ def _run(mass, sel_lens, budget, n_sink=1, n_recent=4, b_max=None):
     return host(sel), host(cnt), ref_sel, ref_cnt
 
 
+# 37 x 8 pairs run one CTA per pair, 80 x 8 one warp per pair (the two kernels of the call)
+@pytest.mark.parametrize("S", [37, 80])
 @pytest.mark.parametrize("budget", [0.0, 0.05, 0.1, 0.25, 0.5, 1.0])
-def test_random_mass_bit_exact(budget):
-    rng = np.random.default_rng(int(budget * 1000))
-    S, H, stride = 37, 8, 1100
+def test_random_mass_bit_exact(budget, S):
+    rng = np.random.default_rng(int(budget * 1000) + S)
+    H, stride = 8, 1100
     sel_lens = rng.integers(0, stride * 16 + 1, size=S)
     sel_lens[:6] = [0, 1, 16, 17, 80, stride * 16]
     mass = rng.gamma(0.5, 1.0, size=(S, H, stride))
@@ -41,9 +43,10 @@ def test_random_mass_bit_exact(budget):
     assert np.array_equal(sel, ref_sel)
 
 
-def test_exact_ties_break_to_lower_page():
+@pytest.mark.parametrize("S", [20, 160])
+def test_exact_ties_break_to_lower_page(S):
     rng = np.random.default_rng(5)
-    S, H, stride = 20, 4, 300
+    H, stride = 4, 300
     sel_lens = rng.integers(1, stride * 16 + 1, size=S)
     mass = rng.integers(0, 3, size=(S, H, stride)).astype(np.float64)   # heavy ties
     for budget in (0.05, 0.3):
