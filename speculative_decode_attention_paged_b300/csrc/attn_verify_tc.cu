@@ -717,8 +717,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         named_bar_sync(kAllBar, kSoftmaxThreads);
         float* dst = a.page_mass + static_cast<int64_t>(pair) * a.mass_stride;
         const float* plse = a.page_lse + static_cast<int64_t>(pair) * a.max_pages * a.R;
-        for (int lp = sm_tid; lp < a.mass_stride; lp += kSoftmaxThreads)
-          dst[lp] = lp < np ? page_mass_of(plse + static_cast<int64_t>(lp) * a.R, row_lse, a.R) : 0.f;
+        if ((a.R & 3) == 0 && a.R <= kTcRows) {
+          // Pages lp and lp + 256 at once: 16 loads of 16 bytes in flight per
+          // thread.  One page at a time left the pipeline stalled for about six
+          // dependent load round trips per pair; three or four pages at once
+          // were slower again (their loads compete with the stage ring's).
+          constexpr int kU = 2;
+          for (int lp0 = sm_tid; lp0 < a.mass_stride; lp0 += kU * kSoftmaxThreads) {
+            float4 v[kU][kTcRows / 4];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              const int lp = lp0 + u * kSoftmaxThreads;
+#pragma unroll
+              for (int q = 0; q < kTcRows / 4; ++q)
+                v[u][q] = (lp < np && 4 * q < a.R)
+                              ? __ldcg(reinterpret_cast<const float4*>(plse + static_cast<int64_t>(lp) * a.R) + q)
+                              : make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              float m = 0.f;
+#pragma unroll
+              for (int q = 0; q < kTcRows / 4; ++q) {
+                const float e[4] = {v[u][q].x, v[u][q].y, v[u][q].z, v[u][q].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float L = 4 * q + k < a.R ? row_lse[4 * q + k] : kNegInf;
+                  if (e[k] != kNegInf && L != kNegInf) m += fast_exp2(e[k] - L);
+                }
+              }
+              const int lp = lp0 + u * kSoftmaxThreads;
+              if (lp < a.mass_stride) dst[lp] = m;
+            }
+          }
+        } else {
+          for (int lp = sm_tid; lp < a.mass_stride; lp += kSoftmaxThreads)
+            dst[lp] = lp < np ? page_mass_of(plse + static_cast<int64_t>(lp) * a.R, row_lse, a.R) : 0.f;
+        }
       }
       ++seg_index;
       named_bar_sync(kAllBar, kSoftmaxThreads);
