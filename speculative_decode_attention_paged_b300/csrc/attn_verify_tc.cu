@@ -532,10 +532,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int pos = (e0 + page) * kPage + (i & 15);
       const bool tok = pos >= lo && pos < hi;
       const int r_min = pos <= Lh ? 0 : (pos - Lh) * a.G;
+      if (tok && r_min == 0 && r0 + kRowsWg <= a.R) {   // the token is visible to all 16 rows
 #pragma unroll
-      for (int j = 0; j < kRowsWg; ++j) {
-        const int r = r0 + j;
-        x[j] = (tok && r >= r_min && r < a.R) ? x[j] * a.scale_log2 : kNegInf;
+        for (int j = 0; j < kRowsWg; ++j) x[j] *= a.scale_log2;
+      } else {
+#pragma unroll
+        for (int j = 0; j < kRowsWg; ++j) {
+          const int r = r0 + j;
+          x[j] = (tok && r >= r_min && r < a.R) ? x[j] * a.scale_log2 : kNegInf;
+        }
       }
 
       // The running max only moves when some score exceeds it by more than
