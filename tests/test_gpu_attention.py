@@ -235,9 +235,15 @@ def _full_round_check(cfg, budget, n_check, seed_q=500):
     torch.cuda.synchronize()
     ws.check()
 
-    # properties at full size: mass rows sum to G*T
+    # properties at full size, every sequence: mass rows sum to G*T, and verify row j
+    # equals a dense decode step over the first L + j + 1 tokens
     G = cfg.q_heads // cfg.kv_heads
     np.testing.assert_allclose(host(mass).astype(np.float64).sum(axis=-1), G * T, rtol=1e-4)
+    for j in range(T):
+        step = torch.empty(qv[:, j].shape, dtype=torch.float32, device=DEV)
+        s3r.s3r_dense_decode_attn(kv_desc(kv), kv.hist_lens + j + 1, qv[:, j].contiguous(), step, 1.0, ws)
+        assert (out_v[:, j] - step).abs().max().item() <= 1e-2, f"{cfg.name} verify row {j} vs dense"
+    ws.check()
 
     seqs = sorted(np.random.default_rng(cfg.seed).choice(cfg.num_seqs, size=n_check, replace=False).tolist())
     kp, vp, bt = compact_pool(kv, seqs)
@@ -268,12 +274,12 @@ def test_tiny_workload_full():
 
 
 def test_qwen3_1p7b_256seq_sampled():
-    _full_round_check(ATTN_QWEN3_1P7B_256SEQ, 0.05, n_check=5)
+    _full_round_check(ATTN_QWEN3_1P7B_256SEQ, 0.05, n_check=24)
 
 
 @pytest.mark.parametrize("budget", [0.05, 0.50])
 def test_qwen3_8b_128seq_sampled(budget):
-    _full_round_check(ATTN_QWEN3_8B_128SEQ, budget, n_check=3)
+    _full_round_check(ATTN_QWEN3_8B_128SEQ, budget, n_check=16)
 
 
 def test_long_context_dense_and_verify_with_mass():

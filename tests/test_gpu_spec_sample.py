@@ -126,7 +126,7 @@ def test_rollout_2048seq_sampled():
         rate = (nacc[:, None] > np.arange(cfg.k)[None, :]).sum() / max(1, (np.minimum(nacc + 1, cfg.k)).sum())
         assert 0.5 < rate < 1.0
         rng = np.random.default_rng(int(sigma * 100))
-        seqs = np.sort(rng.choice(cfg.num_seqs, size=48, replace=False))
+        seqs = np.sort(rng.choice(cfg.num_seqs, size=128, replace=False))
         compare(host(inp.p_logits[seqs]), host(inp.q_logits[seqs]), host(inp.draft_tokens[seqs]),
                 cfg.philox_seed, 0, out[seqs], nacc[seqs], seq_ids=seqs)
 
