@@ -301,7 +301,7 @@ S3R_API s3r_status s3r_spec_sample(const float* p_logits, const float* q_logits,
  * change the result.
  *
  * Same arguments, semantics, results (bit for bit, tie counts included) and
- * workspace size as s3r_spec_sample.  It enqueues k + 3 kernels instead of 4
+ * workspace size as s3r_spec_sample.  It enqueues k + 3 kernels instead of one
  * (plus a clear of tie_count when given) and reads about
  * (2 E[a] + 2) / (2k + 1) of the logit bytes, E[a] the mean accepted count.
  * Its workspace must hold zeroed arrival counters (s3r_workspace_init once

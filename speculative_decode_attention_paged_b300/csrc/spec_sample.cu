@@ -33,9 +33,10 @@
 // With k = 0 there is nothing to test and the row is its own bonus row:
 // bonus_sample streams each row with 4 CTAs, the last of which merges the
 // chunk statistics and picks the token.
-// The sequential variant replaces row_stats + accept by k + 1 launches of
-// seq_step, one per position, which read a sequence's rows only up to its
-// first rejection; chunk_sum and pick follow as above.
+// The sequential variant replaces the row tasks and ratio tests by k + 1
+// launches of seq_step, one per position, which read a sequence's rows only up
+// to its first rejection; chunk_sum and pick then do the chunk sums and the
+// pick as separate launches.
 
 #include <cfloat>
 
@@ -543,8 +544,9 @@ __global__ void __launch_bounds__(kPickThreads)
 // warp per chunk) and stores their (max, sum) pairs; the CTA that arrives
 // last on the sequence's counter (the stores published by a fence before the
 // arrival) merges the pairs, acts for the sequence and resets the counter.
-// The chunk pairs and their merge are those of row_stats, so the row
-// statistics are bitwise the same.
+// The chunk pairs and their merge are those of the one-launch sampler's row
+// tasks (block_chunk_stats, merge_chunk_stats), so the row statistics are
+// bitwise the same on every path.
 
 // This CTA's 8 chunks of row x into dst[kSampleChunks]; true in every thread
 // of the CTA that arrived last among `arrivals_expected` on *counter.
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(kStatThreads)
 // Step i of the sequential (early-exit) ratio tests.  For i < k the rows p_i
 // and q_i of every sequence that has not rejected yet (accept[n] == k) are
 // streamed, kRowParts CTAs each; the last CTA merges both rows' statistics,
-// stores them where row_stats would, and tests draft i.  For i == k the bonus
+// stores them where the one-launch sampler's row tasks do, and tests draft i.  For i == k the bonus
 // row p_k of every sequence that accepted all k drafts is streamed and its
 // chunk statistics kept for the pick.  A sequence is finished at its
 // rejection (or at i == k): accepted drafts, -1 padding and n_accepted are
