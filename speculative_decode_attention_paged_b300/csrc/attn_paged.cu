@@ -414,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need_mask = (elo > page0) || (ehi < page0 + kPage) ||
                              (a.mode == kModeVerify && page0 + kPage - 1 > cur_L);
       uint32_t pa[MT][4], pl[MT][4];
+      float ps_h[MT][2], mu_h[MT][2];   // page mass: this lane's row sums and the max they use
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         float x[2][4];
@@ -454,14 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           l_r[mt][hb] = l_r[mt][hb] * alpha[hb] + psum;
           m_r[mt][hb] = m_new;
-          if (MASS) {
-            const float ps = quad_sum(psum);
-            const int r = mt * 16 + qg + hb * 8;
-            if (qt == 0 && r < a.R) {
-              a.page_lse[(static_cast<int64_t>(cur_pair) * a.max_pages + lp) * a.R + r] =
-                  ps > 0.f ? m_use + fast_log2(ps) : kNegInf;
-            }
-          }
+          ps_h[mt][hb] = psum;
+          mu_h[mt][hb] = m_use;
         }
 #pragma unroll
         for (int n = 0; n < 16; ++n) {
@@ -489,6 +484,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_16816(o[mt][2 * c], pl[mt], b0, b1);
           mma_bf16_16816(o[mt][2 * c + 1], pl[mt], b2, b3);
         }
+      }
+      if (MASS) {
+        // the page's log-sum-exp per row, after the output MMAs are issued
+        float* pg = a.page_lse + (static_cast<int64_t>(cur_pair) * a.max_pages + lp) * a.R;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const float ps = quad_sum(ps_h[mt][hb]);
+            const int r = mt * 16 + qg + hb * 8;
+            if (qt == 0 && r < a.R) pg[r] = ps > 0.f ? mu_h[mt][hb] + fast_log2(ps) : kNegInf;
+          }
       }
     } else if (MASS && lp >= 0) {
       // Nothing visible on this page: it holds no mass.
