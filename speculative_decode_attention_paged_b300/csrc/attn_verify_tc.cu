@@ -532,14 +532,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int pos = (e0 + page) * kPage + (i & 15);
       const bool tok = pos >= lo && pos < hi;
       const int r_min = pos <= Lh ? 0 : (pos - Lh) * a.G;
-      if (tok && r_min == 0 && r0 + kRowsWg <= a.R) {   // the token is visible to all 16 rows
-#pragma unroll
-        for (int j = 0; j < kRowsWg; ++j) x[j] *= a.scale_log2;
-      } else {
+      // x stays unscaled: the scale enters the vote and the exponent by fma
+      if (!(tok && r_min == 0 && r0 + kRowsWg <= a.R)) {   // some row may not see the token
 #pragma unroll
         for (int j = 0; j < kRowsWg; ++j) {
           const int r = r0 + j;
-          x[j] = (tok && r >= r_min && r < a.R) ? x[j] * a.scale_log2 : kNegInf;
+          if (!(tok && r >= r_min && r < a.R)) x[j] = kNegInf;
         }
       }
 
@@ -548,12 +546,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float v[kRowsWg];
       bool exceed = false;
 #pragma unroll
-      for (int j = 0; j < kRowsWg; ++j) exceed |= x[j] > m_run[j] + kRescaleSlack;
+      for (int j = 0; j < kRowsWg; ++j) exceed |= fmaf(x[j], a.scale_log2, -m_run[j]) > kRescaleSlack;
       bool ok_acc = true;
       bool waited_prev = false;
       if (named_bar_or(wg_bar, kWgThreads, exceed)) {
 #pragma unroll
-        for (int j = 0; j < kRowsWg; ++j) v[j] = x[j];
+        for (int j = 0; j < kRowsWg; ++j) v[j] = x[j] * a.scale_log2;
         reduce_scatter<32, kRowsWg, true>(v, lane);   // lanes 2j, 2j+1: row j of this warp
         float* rm = rmax + (t & 1) * 64;
         if ((lane & 1) == 0) rm[q4 * 16 + (lane >> 1)] = v[0];
@@ -599,7 +597,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
 #pragma unroll
       for (int j = 0; j < kRowsWg; ++j) {
-        x[j] = fast_exp2(x[j] - mu[j]);
+        x[j] = fast_exp2(fmaf(x[j], a.scale_log2, -mu[j]));
         l_part[j] += x[j];
       }
       // P^T (bf16 high part and remainder); the buffer is free once PV(t-1) is done
